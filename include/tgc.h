@@ -1,0 +1,279 @@
+/*
+ * tgc.h -- C ABI of libtgc.so: TGATHER row-concat gather and chunked
+ * AllGather fused with a bf16 MatMul, for one sm_103a GPU.
+ *
+ * Sources (web pages):
+ *   [TG]  "CANN PTO-ISA TGATHER 指令深度解析：跨 Rank 行拼接 Gather 的实现原理与开发指南"
+ *   [AGM] "Triton第四课：基于对称内存融合 AllGather 与 MatMul，提速1.56倍"
+ *
+ * Conventions for every entry point
+ *   - Pointers named d_* or documented as "device" are device addresses in the
+ *     current CUDA device; the caller owns them.  Arrays of source pointers
+ *     (srcs, a_shards) are HOST arrays of device pointers; they are copied into
+ *     kernel parameters, so the host array may be freed after the call returns.
+ *   - All work is enqueued on `stream` (cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous unless stated; device buffers must stay alive
+ *     until the stream has passed the call.
+ *   - Tensors are dense and row-major (C order).
+ *   - Argument errors are reported synchronously as a negative tgc_status
+ *     before anything is enqueued.  Errors detected on the device (a bounded
+ *     wait that expired) are written to a device status word; the synchronous
+ *     entry points read it back and return it.
+ *   - The library keeps no state between calls (tensor descriptors are
+ *     encoded per call on the host).  It is safe to call from several host
+ *     threads.
+ *   - A "virtual rank" is one of `nranks` separate allocations in the same
+ *     GPU's memory standing for the shard a rank holds ([AGM] section
+ *     对称内存如何打通GPU间访问: every rank holds a_shard of shape (M/W, K)).
+ */
+#ifndef TGC_H
+#define TGC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TGC_MAX_RANKS 64
+
+typedef enum tgc_status {
+    TGC_OK = 0,
+    TGC_ERR_INVALID_ARG = -1,  /* null pointer, bad count or shape, bad mode   */
+    TGC_ERR_DTYPE = -2,        /* unknown dtype                               */
+    TGC_ERR_ALIGN = -3,        /* pointer or row pitch misaligned for the path */
+    TGC_ERR_NOT_RESIDENT = -4, /* the persistent grid cannot be made resident */
+    TGC_ERR_CUDA = -5,         /* a CUDA call failed: see tgc_last_cuda_error */
+    TGC_ERR_TIMEOUT = -6,      /* a bounded device wait expired               */
+    TGC_ERR_ABORTED = -7,      /* the kernel stopped because another CTA timed out */
+    TGC_ERR_WORKSPACE = -8     /* workspace missing or too small              */
+} tgc_status;
+
+/* Element types.  TGATHER only uses the element size ([TG] §7.1: source,
+ * destination and staging tile share one type; the copy is type-agnostic). */
+typedef enum tgc_dtype {
+    TGC_U8 = 0, TGC_I8 = 1, TGC_F16 = 2, TGC_BF16 = 3,
+    TGC_I32 = 4, TGC_F32 = 5, TGC_I64 = 6, TGC_F64 = 7
+} tgc_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* TGATHER                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tgc_tgather -- [TG] §二 数学语义:
+ *     dst[d0, d1, d2, r*H + i, j] = srcs[r][d0, d1, d2, i, j]
+ *     for r in [0, nranks), i in [0, H), j in [0, W), every (d0, d1, d2).
+ *
+ * dst     device, (D0, D1, D2, nranks*H, W) elements of `dtype`, written.
+ * srcs    host array of nranks device pointers, each (D0, D1, D2, H, W),
+ *         read.  All sources share shape and layout ([TG] §7.3).
+ * dtype   element type (only its size matters).
+ * Alignment: every pointer must be aligned to the element size.  Any H and W
+ * are accepted (non-tile-multiple tails are handled; [TG] §7.4's divisibility
+ * rule for static tiles does not apply).
+ * Empty input (any of D0, D1, D2, H, W == 0) returns TGC_OK and writes
+ * nothing ([TG] §七: empty data returns before any transfer).
+ * Errors: TGC_ERR_INVALID_ARG (nranks not in [1, TGC_MAX_RANKS], negative
+ * extent, null pointer), TGC_ERR_DTYPE, TGC_ERR_ALIGN, TGC_ERR_CUDA.
+ * Asynchronous on `stream`.
+ */
+int tgc_tgather(void *dst, const void *const *srcs, int nranks,
+                int64_t D0, int64_t D1, int64_t D2, int64_t H, int64_t W,
+                tgc_dtype dtype, cudaStream_t stream);
+
+/*
+ * Extended TGATHER.  Adds:
+ *   dst_rows3  dst's DIM_3; 0 means nranks*H.  [TG] §7.2: it may exceed
+ *              nranks*H, in which case only the first nranks*H rows of each
+ *              (d0, d1, d2) slab are written and the rest are left unchanged.
+ *   progress   optional device uint32 array of nranks*S entries,
+ *              S = ceil(H / chunk_rows).  Entry c = r*S + s refers to rows
+ *              [s*chunk_rows, min((s+1)*chunk_rows, H)) of rank r in every
+ *              slab.  When all those rows are in dst, the kernel stores
+ *              `epoch` there with a gpu-scope release ([AGM] section
+ *              数据搬运与细粒度同步: one progress entry per (src_rank,
+ *              split_id) at offset src_rank*splits_per_rank + split_id; the
+ *              data must be visible before the flag).  A reader that loads the
+ *              entry with gpu-scope acquire and sees `epoch` may read the rows.
+ *   counters   device uint32 array of nranks*S entries, required with
+ *              progress; must be zero on entry and is zero again when the
+ *              kernel ends.
+ *   chunk_rows rows per progress chunk (> 0 when progress is given).
+ *   epoch      the value published; must differ from every value the
+ *              progress entries hold on entry ([AGM] same section, last
+ *              paragraph: versioned progress values keep a previous round's
+ *              flag from passing as a new one).
+ */
+typedef struct tgc_tgather_args {
+    void *dst;
+    const void *const *srcs;
+    int nranks;
+    int64_t D0, D1, D2, H, W;
+    tgc_dtype dtype;
+    int64_t dst_rows3;
+    uint32_t *progress;
+    uint32_t *counters;
+    int64_t chunk_rows;
+    uint32_t epoch;
+    cudaStream_t stream;
+} tgc_tgather_args;
+
+int tgc_tgather_ex(const tgc_tgather_args *args);
+
+/* ------------------------------------------------------------------------ */
+/* AllGather fused with MatMul                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tgc_ag_matmul -- [AGM]: gather nranks shards along M into `a` and compute
+ *     C = a * B^T   (a: (M, K), B stored (N, K), C: (M, N); bf16 in and out,
+ *                    fp32 accumulation)
+ * with the gather cut into communication blocks of comm_block_rows rows, each
+ * published through a progress flag, and the MatMul tiles consuming each
+ * block as soon as its flag is set ([AGM] sections 融合后的流水线 and
+ * MatMul 按需等待远端分片).  The result equals gather-then-MatMul.
+ *
+ * a_shards        host array of nranks device pointers, each (M/nranks, K)
+ *                 bf16, 16-byte aligned.
+ * B               device (N, K) bf16, 16-byte aligned.
+ * C               device (M, N) bf16, written.
+ * comm_block_rows must divide M/nranks.
+ * Requirements: M % nranks == 0, K % 8 == 0 and N % 8 == 0 (16-byte rows for
+ * TMA), K > 0.
+ * Temporaries (`a`, progress flags, workspace) are allocated stream-ordered
+ * from a memory pool the library creates per device (cudaMallocFromPoolAsync)
+ * and freed the same way; the pool keeps freed memory for the next call.  This entry point synchronizes
+ * `stream` before returning so that it can report a device-side error.
+ * M == 0 or N == 0: returns TGC_OK, nothing written.
+ */
+int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *C,
+                  int64_t M, int64_t K, int64_t N, int64_t comm_block_rows,
+                  cudaStream_t stream);
+
+typedef enum tgc_mode {
+    TGC_MODE_FUSED = 0,   /* one kernel: copy blocks into a_out + flag-waiting GEMM */
+    TGC_MODE_UNFUSED = 1, /* tgather kernel into a_out, then the GEMM kernel on a_out */
+    TGC_MODE_MM_ONLY = 2  /* GEMM kernel on a_out as it is (every block taken as ready) */
+} tgc_mode;
+
+/*
+ * Tile order.  Tiles are first grouped along M in groups of `group_m` tile
+ * rows (the usual L2-friendly swizzle), then pid_m is rotated
+ * ([AGM] section 融合后的流水线: the pivot is applied after the swizzle):
+ *   PAGE : pid_m = (pid_m + floor(rank*comm_block_rows / BM)) % num_pid_m,
+ *          the page's (pid_m + NUM_PID_M_PER_COMM_BLOCK*RANK) % num_pid_m
+ *          whenever BM divides comm_block_rows;
+ *   SHARD: pid_m = (pid_m + floor(rank*(M/nranks) / BM)) % num_pid_m, which
+ *          starts every rank on its own shard;
+ *   NONE : no rotation.
+ * The pivot only reorders tiles; C does not depend on it.
+ */
+typedef enum tgc_pivot {
+    TGC_PIVOT_PAGE = 0,
+    TGC_PIVOT_SHARD = 1,
+    TGC_PIVOT_NONE = 2
+} tgc_pivot;
+
+/*
+ * Extended AllGather-MatMul.  Fields beyond tgc_ag_matmul's:
+ *   a_out        device (M, K) bf16: the gathered A.  FUSED and UNFUSED write
+ *                it completely (local shard included); MM_ONLY reads it.
+ *   rank         the calling virtual rank, 0 <= rank < nranks.  Tiles whose
+ *                rows lie inside shard `rank` read a_shards[rank] directly
+ *                and wait for nothing; all other tiles wait for the flags of
+ *                every block they cover and read a_out.
+ *   progress     device uint32 array of M/comm_block_rows entries; block
+ *                c = src_rank*S + split_id, S = (M/nranks)/comm_block_rows.
+ *                FUSED stores `epoch` into entry c with a gpu-scope release
+ *                once block c is in a_out.  Unused by UNFUSED/MM_ONLY.
+ *   epoch        must differ from every value progress holds on entry.
+ *   order        optional HOST int32 array of n_order distinct block ids in
+ *                [0, M/comm_block_rows): the order in which the producer
+ *                copies and releases blocks (copied into the workspace).
+ *                NULL: the order in which the tile schedule first reaches the
+ *                blocks' rows, the caller's own shard last (its tiles read the
+ *                shard directly).  Blocks missing from `order` are never
+ *                released: their tiles wait until spin_timeout_ns and the call
+ *                fails with TGC_ERR_TIMEOUT (host-side fault injection).
+ *   delay_ns     optional HOST uint32 array, one entry per block: the
+ *                producer that completes a block busy-waits that many ns on
+ *                %globaltimer before it publishes the block (injected arrival
+ *                skew).
+ *   spin_timeout_ns  limit for every device wait; 0 = 2 s.
+ *   group_m      tile rows per swizzle group; 0 = default (8).
+ *   grid         persistent CTAs; 0 = one per SM.
+ *   workspace    device memory of tgc_ag_matmul_workspace_bytes() bytes,
+ *                128-byte aligned, zero-filled once by the caller before first
+ *                use; every call that succeeds leaves its counters and status
+ *                zeroed again (after an error, zero it again).  Required by
+ *                FUSED; optional otherwise.
+ *   d_status     optional device int32, zeroed by the call, then set by the
+ *                kernel to a tgc_status code if a device wait fails.  When
+ *                NULL the status word lives in the workspace (FUSED) or is
+ *                not kept (UNFUSED / MM_ONLY without workspace).
+ *   sync         nonzero: synchronize `stream` and return the device status.
+ * Calls that share a workspace or progress array must not overlap on the GPU.
+ */
+typedef struct tgc_ag_matmul_args {
+    const void *const *a_shards;
+    int nranks;
+    const void *B;
+    void *C;
+    void *a_out;
+    int64_t M, K, N;
+    int64_t comm_block_rows;
+    int rank;
+    tgc_mode mode;
+    tgc_pivot pivot;
+    uint32_t *progress;
+    uint32_t epoch;
+    const int32_t *order;
+    int64_t n_order;
+    const uint32_t *delay_ns;
+    uint64_t spin_timeout_ns;
+    int group_m;
+    int grid;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *d_status;
+    int sync;
+    cudaStream_t stream;
+} tgc_ag_matmul_args;
+
+int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
+
+/* Bytes of workspace tgc_ag_matmul_ex needs for this problem (>= 256). */
+size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N,
+                                     int64_t comm_block_rows);
+
+/*
+ * Host-side copy of the tile schedule the GEMM kernels run (the same code the
+ * device uses): writes, for persistent CTA `cta` of `grid`, the sequence of
+ * (pid_m, pid_n) pairs it processes into out[2*t], out[2*t+1], at most
+ * max_tiles pairs; returns the number of tiles of that CTA, or a negative
+ * tgc_status.  Needs no GPU.
+ */
+int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks,
+                               int rank, tgc_pivot pivot, int group_m, int grid, int cta,
+                               int64_t *out, int64_t max_tiles);
+
+/* Tile shape used by the GEMM kernels (BM, BN, BK). */
+void tgc_gemm_tile_shape(int *bm, int *bn, int *bk);
+
+/* ------------------------------------------------------------------------ */
+/* Misc                                                                      */
+/* ------------------------------------------------------------------------ */
+
+const char *tgc_status_string(int status);
+/* Last CUDA error seen by this thread inside the library (cudaSuccess if none). */
+int tgc_last_cuda_error(void);
+/* Library version, e.g. "0.1.0". */
+const char *tgc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TGC_H */

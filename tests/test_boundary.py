@@ -1,0 +1,196 @@
+"""C-ABI boundary tests that need no GPU: the library loads, exports every
+symbol include/tgc.h declares, rejects invalid arguments synchronously (before
+any CUDA call), returns early on empty work, and its host-side copy of the
+tile schedule has the properties the pages require of the pivot."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tile_gather_comm_gb300 as tgc
+from tile_gather_comm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tgc.h")
+FAKE = 1 << 20  # a 1 MiB-aligned fake device address: never dereferenced on these paths
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from tile_gather_comm_gb300 import _build
+    _build.build()
+
+
+def _declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tgc_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert len(names) >= 10
+    L = _lib.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version():
+    assert tgc.tgc_status_string(0) == "ok"
+    assert "wait" in tgc.tgc_status_string(_lib.TGC_ERR_TIMEOUT)
+    assert tgc.tgc_status_string(12345) == "unknown status"
+    assert tgc.tgc_version().count(".") == 2
+    assert tgc.tgc_gemm_tile_shape() == (128, 256, 64)
+
+
+def _tg(dst, srcs, n, D0, D1, D2, H, W, dt=5):
+    arr = (ctypes.c_void_p * max(1, n))(*srcs)
+    return _lib.lib().tgc_tgather(dst, arr, n, D0, D1, D2, H, W, dt, None)
+
+
+def test_tgather_invalid_arguments():
+    E = _lib
+    assert _tg(FAKE, [FAKE], 0, 1, 1, 1, 1, 1) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE] * 65, 65, 1, 1, 1, 1, 1) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE], 1, -1, 1, 1, 1, 1) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE], 1, 1, 1, 1, 1, -4) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE], 1, 1, 1, 1, 1, 1, dt=99) == E.TGC_ERR_DTYPE
+    assert _tg(None, [FAKE], 1, 1, 1, 1, 4, 4) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [None], 1, 1, 1, 1, 4, 4) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE + 2, [FAKE], 1, 1, 1, 1, 4, 4, dt=5) == E.TGC_ERR_ALIGN   # f32 needs 4-byte alignment
+    assert _tg(FAKE, [FAKE, FAKE + 6], 2, 1, 1, 1, 4, 4, dt=6) == E.TGC_ERR_ALIGN
+
+
+@pytest.mark.parametrize("shape", [(0, 1, 1, 4, 4), (1, 0, 1, 4, 4), (1, 1, 0, 4, 4), (1, 1, 1, 0, 4), (1, 1, 1, 4, 0)])
+def test_tgather_empty_returns_ok_without_touching_memory(shape):
+    # null pointers prove that nothing is dereferenced or launched
+    assert _tg(None, [None, None], 2, *shape) == _lib.TGC_OK
+
+
+def test_tgather_ex_rejects_short_dst_and_missing_counters():
+    L = _lib.lib()
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    a = _lib.TgatherArgs(dst=FAKE, srcs=arr, nranks=2, D0=1, D1=1, D2=1, H=4, W=4, dtype=5, dst_rows3=7)
+    assert L.tgc_tgather_ex(ctypes.byref(a)) == _lib.TGC_ERR_INVALID_ARG
+    a = _lib.TgatherArgs(dst=FAKE, srcs=arr, nranks=2, D0=1, D1=1, D2=1, H=4, W=4, dtype=5,
+                         progress=FAKE, counters=None, chunk_rows=2)
+    assert L.tgc_tgather_ex(ctypes.byref(a)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_tgather_ex(None) == _lib.TGC_ERR_INVALID_ARG
+
+
+def _ag(**kw):
+    R = kw.pop("R", 4)
+    args = dict(a_shards=(ctypes.c_void_p * R)(*([FAKE] * R)), nranks=R, B=FAKE, C=FAKE, a_out=FAKE,
+                M=64, K=64, N=64, comm_block_rows=8, rank=0, mode=0, pivot=0, progress=FAKE, epoch=1,
+                workspace=FAKE, workspace_bytes=1 << 20, sync=0)
+    args.update(kw)
+    return _lib.lib().tgc_ag_matmul_ex(ctypes.byref(_lib.AgMatmulArgs(**args)))
+
+
+def test_ag_matmul_invalid_arguments():
+    E = _lib
+    assert _ag(nranks=0) == E.TGC_ERR_INVALID_ARG
+    assert _ag(M=66) == E.TGC_ERR_INVALID_ARG            # M % R != 0
+    assert _ag(comm_block_rows=5) == E.TGC_ERR_INVALID_ARG  # cb does not divide M/R
+    assert _ag(comm_block_rows=0) == E.TGC_ERR_INVALID_ARG
+    assert _ag(rank=4) == E.TGC_ERR_INVALID_ARG
+    assert _ag(rank=-1) == E.TGC_ERR_INVALID_ARG
+    assert _ag(mode=7) == E.TGC_ERR_INVALID_ARG
+    assert _ag(pivot=9) == E.TGC_ERR_INVALID_ARG
+    assert _ag(K=60) == E.TGC_ERR_ALIGN                   # 16-byte rows for TMA
+    assert _ag(N=60) == E.TGC_ERR_ALIGN
+    assert _ag(K=0) == E.TGC_ERR_INVALID_ARG
+    assert _ag(B=FAKE + 8) == E.TGC_ERR_ALIGN
+    assert _ag(C=None) == E.TGC_ERR_INVALID_ARG
+    assert _ag(progress=None) == E.TGC_ERR_INVALID_ARG
+    assert _ag(workspace=None) == E.TGC_ERR_WORKSPACE
+    assert _ag(workspace_bytes=16) == E.TGC_ERR_WORKSPACE
+    R = 4
+    bad = (ctypes.c_void_p * R)(FAKE, FAKE, FAKE + 4, FAKE)
+    assert _ag(a_shards=bad) == E.TGC_ERR_ALIGN
+    dup = (ctypes.c_int32 * 3)(0, 1, 1)
+    assert _ag(order=dup, n_order=3) == E.TGC_ERR_INVALID_ARG
+    oob = (ctypes.c_int32 * 2)(0, 8)
+    assert _ag(order=oob, n_order=2) == E.TGC_ERR_INVALID_ARG
+    assert _lib.lib().tgc_ag_matmul_ex(None) == E.TGC_ERR_INVALID_ARG
+
+
+def test_ag_matmul_empty_problem_is_ok():
+    assert _ag(M=0, B=None, C=None, a_out=None) == _lib.TGC_OK
+    assert _ag(N=0, B=None, C=None, a_out=None) == _lib.TGC_OK
+    arr = (ctypes.c_void_p * 2)(None, None)
+    assert _lib.lib().tgc_ag_matmul(arr, 2, None, None, 0, 64, 64, 8, None) == _lib.TGC_OK
+
+
+def test_plain_ag_matmul_validates_before_allocating():
+    arr = (ctypes.c_void_p * 4)(*([FAKE] * 4))
+    L = _lib.lib()
+    assert L.tgc_ag_matmul(arr, 4, FAKE, FAKE, 66, 64, 64, 8, None) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_ag_matmul(arr, 4, FAKE, FAKE, 64, 60, 64, 8, None) == _lib.TGC_ERR_ALIGN
+
+
+def test_workspace_bytes_grows_with_blocks():
+    a = tgc.tgc_ag_matmul_workspace_bytes(4, 64, 64, 64, 8)
+    b = tgc.tgc_ag_matmul_workspace_bytes(4, 32768, 8192, 8192, 512)
+    c = tgc.tgc_ag_matmul_workspace_bytes(8, 1 << 20, 64, 64, 8)
+    assert 256 <= a <= b < c
+
+
+# ----------------------------------------------------------------------------- schedule
+
+
+def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0):
+    seqs = [tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, pivot, group_m, grid, c) for c in range(grid)]
+    return seqs
+
+
+@pytest.mark.parametrize("M,N,cb,R", [(4096, 4096, 128, 8), (8192, 14336, 256, 8), (32768, 8192, 512, 4),
+                                      (64, 64, 8, 4), (1000 * 8, 1000, 1000, 8)])
+@pytest.mark.parametrize("pivot", ["page", "shard", "none"])
+def test_schedule_is_a_permutation(M, N, cb, R, pivot):
+    bm, bn, _ = tgc.tgc_gemm_tile_shape()
+    npm, npn = -(-M // bm), -(-N // bn)
+    for rank in sorted({0, 1, R - 1}):
+        seqs = _all_tiles(M, N, cb, R, rank, pivot, grid=148)
+        tiles = [t for s in seqs for t in s]
+        assert len(tiles) == npm * npn
+        assert len(set(tiles)) == npm * npn
+        assert all(0 <= pm < npm and 0 <= pn < npn for pm, pn in tiles)
+
+
+@pytest.mark.parametrize("M,N,cb,R", [(4096, 4096, 512, 8), (32768, 8192, 8192, 4)])
+def test_page_pivot_matches_formula_and_starts_on_local_shard_when_one_block_per_rank(M, N, cb, R):
+    """Triton第四课 (融合后的流水线): pid_m = (pid_m + NUM_PID_M_PER_COMM_BLOCK*RANK) % num_pid_m
+    after the GROUP_SIZE_M swizzle; with one comm block per rank every rank begins on its own
+    shard."""
+    bm, bn, _ = tgc.tgc_gemm_tile_shape()
+    npm, npn = M // bm, -(-N // bn)
+    tpb = cb // bm
+    G = 8
+    for rank in range(R):
+        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", G, 1, 0)
+        for t, (pm, pn) in enumerate(seq):
+            group = t // (G * npn)
+            first = group * G
+            gsz = min(npm - first, G)
+            pm0 = first + (t % (G * npn)) % gsz
+            pn0 = (t % (G * npn)) // gsz
+            assert (pm, pn) == ((pm0 + tpb * rank) % npm, pn0)
+        assert seq[0][0] * bm // (M // R) == rank
+
+
+def test_shard_pivot_starts_every_rank_on_its_shard():
+    M, N, cb, R = 8192, 14336, 256, 8
+    bm = tgc.tgc_gemm_tile_shape()[0]
+    for rank in range(R):
+        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "shard", 8, 1, 0)
+        assert seq[0][0] * bm // (M // R) == rank
+
+
+def test_schedule_rejects_bad_arguments():
+    with pytest.raises(tgc.TGCError):
+        tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 4, "page", 8, 1, 0)
+    with pytest.raises(tgc.TGCError):
+        tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 0, "page", 8, 2, 2)

@@ -1,0 +1,133 @@
+"""TGATHER on the GPU against the CPU oracle, bit for bit.
+
+Covers the pages' workloads (tiny fp32, 8 x fp16 (2,1,1,1024,1024), ragged
+int32 (1000, 777)), the TGATHER page's test table (§九), element sizes 1..8,
+D0..D2 > 1, misaligned sources (narrower vectors and peeled heads/tails), a
+destination with DIM_3 > N*H (§7.2), empty inputs (§七) and per-chunk
+progress release.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tile_gather_comm_gb300 as tgc
+from tile_gather_comm_gb300.workloads import TG_CONFIGS, make_tg_inputs
+
+from .helpers import requires_gpu
+from .test_oracle_pins import _golden_cases, _tagged_sources
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    requires_gpu()
+
+
+def _bytes(t):
+    return t.detach().cpu().contiguous().numpy().tobytes()
+
+
+@pytest.mark.parametrize("name", list(TG_CONFIGS))
+def test_workloads_bit_exact(name):
+    cfg = TG_CONFIGS[name]
+    srcs = make_tg_inputs(cfg, seed=0)
+    D0, D1, D2, H, W = cfg.shape
+    d_srcs = [s.to(DEV) for s in srcs]
+    dst = torch.empty((D0, D1, D2, cfg.nranks * H, W), dtype=cfg.dtype, device=DEV)
+    dst.view(torch.uint8).fill_(0xA5)
+    tgc.tgc_tgather(dst, d_srcs)
+    ref = oracle.tgather([s.numpy() for s in srcs])
+    assert _bytes(dst) == ref.tobytes()
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c[0])
+@pytest.mark.parametrize("nranks", [1, 2, 4, 8])
+def test_page_test_table(case, nranks):
+    name, dt, rows, cols, _ = case
+    srcs = _tagged_sources(dt, rows, cols, nranks)
+    d_srcs = [torch.from_numpy(s).to(DEV) for s in srcs]
+    # two spare destination rows (DIM_3 > N*H) must keep their -1 fill in every case,
+    # including the empty one, where nothing at all may be written
+    rows3 = nranks * rows + 2
+    prefill = np.full((1, 1, 1, rows3, cols), -1).astype(srcs[0].dtype)
+    dst = torch.from_numpy(prefill.copy()).to(DEV)
+    tgc.tgc_tgather_ex(dst, d_srcs, dst_rows3=rows3)
+    ref = oracle.tgather(srcs, dst_rows3=rows3, dst=prefill)
+    assert _bytes(dst) == ref.tobytes()
+    assert np.all(dst.cpu().numpy()[0, 0, 0, nranks * rows:].astype(np.int64) % 256 == 255)
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 2, 5, 7), (1, 1, 1, 1, 1), (3, 1, 2, 33, 65), (1, 2, 1, 257, 129),
+                                   (2, 1, 1, 1024, 24)])
+@pytest.mark.parametrize("dtype", [torch.uint8, torch.float16, torch.int32, torch.float64])
+@pytest.mark.parametrize("nranks", [1, 3, 8])
+def test_shapes_and_dtypes(shape, dtype, nranks):
+    es = torch.empty((), dtype=dtype).element_size()
+    g = torch.Generator().manual_seed(nranks * 7 + es)
+    srcs = [torch.randint(0, 256, shape + (es,), generator=g, dtype=torch.uint8).view(dtype).reshape(shape)
+            for _ in range(nranks)]
+    d_srcs = [s.to(DEV) for s in srcs]
+    dst = torch.zeros(shape[:3] + (nranks * shape[3], shape[4]), dtype=dtype, device=DEV)
+    tgc.tgc_tgather(dst, d_srcs)
+    assert _bytes(dst) == _bytes(torch.cat(srcs, dim=3))
+
+
+@pytest.mark.parametrize("src_off,dst_off", [(1, 0), (0, 3), (2, 6), (5, 1), (4, 4)])
+def test_misaligned_pointers(src_off, dst_off):
+    """Sources and destination at element offsets that break 16-byte alignment."""
+    shape = (2, 1, 1, 37, 41)
+    nranks = 4
+    n = int(np.prod(shape))
+    g = torch.Generator().manual_seed(src_off * 10 + dst_off)
+    bufs = [torch.randint(-2**31, 2**31, (n + 16,), generator=g, dtype=torch.int64).to(torch.int32).to(DEV)
+            for _ in range(nranks)]
+    srcs = [b[src_off + r:src_off + r + n].view(shape) for r, b in enumerate(bufs)]
+    big = torch.zeros(nranks * n + 16, dtype=torch.int32, device=DEV)
+    dst = big[dst_off:dst_off + nranks * n].view(shape[:3] + (nranks * shape[3], shape[4]))
+    tgc.tgc_tgather(dst, srcs)
+    ref = oracle.tgather([s.cpu().numpy() for s in srcs])
+    assert _bytes(dst) == ref.tobytes()
+    assert torch.all(big[:dst_off] == 0) and torch.all(big[dst_off + nranks * n:] == 0)
+
+
+def test_dst_rows3_larger_leaves_rest():
+    shape = (2, 1, 2, 30, 17)
+    srcs = [torch.randn(shape) for _ in range(3)]
+    rows3 = 3 * 30 + 11
+    dst = torch.full(shape[:3] + (rows3, 17), -7.0, device=DEV)
+    tgc.tgc_tgather_ex(dst, [s.to(DEV) for s in srcs], dst_rows3=rows3)
+    ref = oracle.tgather([s.numpy() for s in srcs], dst_rows3=rows3,
+                         dst=np.full(shape[:3] + (rows3, 17), -7.0, dtype=np.float32))
+    assert _bytes(dst) == ref.tobytes()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 0, 8), (1, 1, 1, 8, 0), (0, 1, 1, 8, 8)])
+def test_empty_leaves_dst(shape):
+    D0, D1, D2, H, W = shape
+    srcs = [torch.zeros(shape, device=DEV) for _ in range(2)]
+    dst = torch.full((max(D0, 1), D1, D2, max(2 * H, 1), max(W, 1)), -1.0, device=DEV)
+    tgc.tgc_tgather(dst, srcs)
+    torch.cuda.synchronize()
+    assert torch.all(dst == -1)
+
+
+@pytest.mark.parametrize("H,W,chunk_rows,D0", [(1024, 1024, 128, 2), (1000, 777, 96, 1), (64, 32, 7, 3)])
+def test_progress_release(H, W, chunk_rows, D0):
+    nranks = 8
+    shape = (D0, 1, 1, H, W)
+    g = torch.Generator().manual_seed(H + W)
+    srcs = [torch.randint(-2**31, 2**31, shape, generator=g, dtype=torch.int64).to(torch.int32)
+            for _ in range(nranks)]
+    S = -(-H // chunk_rows)
+    progress = torch.full((nranks * S,), 6, dtype=torch.int32, device=DEV)   # stale epoch
+    counters = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    dst = torch.zeros((D0, 1, 1, nranks * H, W), dtype=torch.int32, device=DEV)
+    tgc.tgc_tgather_ex(dst, [s.to(DEV) for s in srcs], progress=progress, counters=counters,
+                       chunk_rows=chunk_rows, epoch=7)
+    torch.cuda.synchronize()
+    assert _bytes(dst) == oracle.tgather([s.numpy() for s in srcs]).tobytes()
+    assert torch.all(progress == 7)
+    assert torch.all(counters == 0)

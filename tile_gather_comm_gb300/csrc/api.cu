@@ -1,0 +1,438 @@
+// api.cu -- the C ABI of libtgc.so (declared in include/tgc.h): argument
+// validation, workspace layout, and the launch sequence of each mode.
+// Every check runs before anything is enqueued, so invalid calls return
+// synchronously and touch no device state.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "schedule.h"
+
+namespace tgc {
+
+static thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return TGC_ERR_CUDA;
+}
+
+int sm_count(int device) {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= device) cache.resize(device + 1, 0);
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 1;
+        cache[device] = n;
+    }
+    return cache[device];
+}
+
+WorkspaceLayout workspace_layout(int64_t nblocks) {
+    WorkspaceLayout w{};
+    auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
+    w.status_off = 0;
+    w.tickets_off = 64;
+    w.counters_off = 128;
+    size_t off = w.counters_off + up((size_t)nblocks * 4, 128);
+    w.order_off = off;
+    off += up((size_t)nblocks * 4, 128);
+    w.delay_off = off;
+    off += up((size_t)nblocks * 4, 128);
+    w.total = off < 256 ? 256 : off;
+    return w;
+}
+
+static int elem_size(tgc_dtype dt) {
+    switch (dt) {
+        case TGC_U8: case TGC_I8: return 1;
+        case TGC_F16: case TGC_BF16: return 2;
+        case TGC_I32: case TGC_F32: return 4;
+        case TGC_I64: case TGC_F64: return 8;
+        default: return 0;
+    }
+}
+
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Memory pool of the allocating entry point, one per device, owned by the
+// library so that its release threshold does not change the device's default
+// pool.  Memory freed back to it stays mapped for the next call.
+static cudaError_t library_pool(int device, cudaMemPool_t *out) {
+    static std::mutex mu;
+    static std::vector<cudaMemPool_t> pools;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)pools.size() <= device) pools.resize(device + 1, nullptr);
+    if (pools[device] == nullptr) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t pool = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) return e;
+        pools[device] = pool;
+    }
+    *out = pools[device];
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ TGATHER
+
+static int tgather_impl(const tgc_tgather_args &a) {
+    if (a.nranks <= 0 || a.nranks > TGC_MAX_RANKS) return TGC_ERR_INVALID_ARG;
+    if (a.D0 < 0 || a.D1 < 0 || a.D2 < 0 || a.H < 0 || a.W < 0 || a.dst_rows3 < 0) return TGC_ERR_INVALID_ARG;
+    const int es = elem_size(a.dtype);
+    if (es == 0) return TGC_ERR_DTYPE;
+    const int64_t rows3 = a.dst_rows3 == 0 ? (int64_t)a.nranks * a.H : a.dst_rows3;
+    if (rows3 < (int64_t)a.nranks * a.H) return TGC_ERR_INVALID_ARG;
+    if (a.progress != nullptr && (a.counters == nullptr || a.chunk_rows <= 0)) return TGC_ERR_INVALID_ARG;
+    const int64_t nslab = a.D0 * a.D1 * a.D2;
+    if (nslab == 0 || a.H == 0 || a.W == 0) return TGC_OK;  // empty: early return, nothing written
+    if (a.dst == nullptr || a.srcs == nullptr) return TGC_ERR_INVALID_ARG;
+    for (int r = 0; r < a.nranks; ++r)
+        if (a.srcs[r] == nullptr) return TGC_ERR_INVALID_ARG;
+    if (!aligned(a.dst, es)) return TGC_ERR_ALIGN;
+    for (int r = 0; r < a.nranks; ++r)
+        if (!aligned(a.srcs[r], es)) return TGC_ERR_ALIGN;
+    if (a.progress != nullptr && (!aligned(a.progress, 4) || !aligned(a.counters, 4))) return TGC_ERR_ALIGN;
+
+    TGatherLaunch L{};
+    for (int r = 0; r < a.nranks; ++r) L.srcs[r] = a.srcs[r];
+    L.dst = a.dst;
+    L.nranks = a.nranks;
+    L.es = es;
+    L.nslab = nslab;
+    L.run_bytes = a.H * a.W * es;
+    L.dst_slab_bytes = rows3 * a.W * es;
+    if (a.progress != nullptr) {
+        const int64_t cr = a.chunk_rows < a.H ? a.chunk_rows : a.H;
+        L.seg_bytes = cr * a.W * es;
+        L.nseg = (a.H + cr - 1) / cr;
+        L.progress = a.progress;
+        L.counters = a.counters;
+        L.epoch = a.epoch;
+    } else {
+        L.seg_bytes = L.run_bytes;
+        L.nseg = 1;
+    }
+    return launch_tgather(L, a.stream);
+}
+
+// ------------------------------------------------------------------ AG-MatMul
+
+struct AGCheck {
+    int64_t nblocks;
+    int64_t rows_per_rank;
+};
+
+static int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
+    if (a.nranks <= 0 || a.nranks > TGC_MAX_RANKS) return TGC_ERR_INVALID_ARG;
+    if (a.M < 0 || a.K < 0 || a.N < 0) return TGC_ERR_INVALID_ARG;
+    if (a.mode != TGC_MODE_FUSED && a.mode != TGC_MODE_UNFUSED && a.mode != TGC_MODE_MM_ONLY)
+        return TGC_ERR_INVALID_ARG;
+    if (a.pivot != TGC_PIVOT_PAGE && a.pivot != TGC_PIVOT_SHARD && a.pivot != TGC_PIVOT_NONE)
+        return TGC_ERR_INVALID_ARG;
+    if (a.M % a.nranks != 0) return TGC_ERR_INVALID_ARG;
+    const int64_t rows_per_rank = a.M / a.nranks;
+    if (a.mode == TGC_MODE_FUSED) {
+        if (a.comm_block_rows <= 0) return TGC_ERR_INVALID_ARG;
+        if (rows_per_rank % a.comm_block_rows != 0) return TGC_ERR_INVALID_ARG;
+    }
+    if (a.rank < 0 || a.rank >= a.nranks) return TGC_ERR_INVALID_ARG;
+    if (a.group_m < 0 || a.grid < 0) return TGC_ERR_INVALID_ARG;
+    // sizes the kernels index with 32-bit integers
+    if (a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 31))
+        return TGC_ERR_INVALID_ARG;
+    out.rows_per_rank = rows_per_rank;
+    out.nblocks = a.mode == TGC_MODE_FUSED ? a.M / a.comm_block_rows : 0;
+    if (a.M == 0 || a.N == 0) return 1;  // nothing to do
+    if (a.K == 0) return TGC_ERR_INVALID_ARG;
+    if (a.K % 8 != 0 || a.N % 8 != 0) return TGC_ERR_ALIGN;
+    if (a.B == nullptr || a.C == nullptr || a.a_out == nullptr) return TGC_ERR_INVALID_ARG;
+    if (!aligned(a.B, 16) || !aligned(a.C, 16) || !aligned(a.a_out, 16)) return TGC_ERR_ALIGN;
+    if (a.mode != TGC_MODE_MM_ONLY) {
+        if (a.a_shards == nullptr) return TGC_ERR_INVALID_ARG;
+        for (int r = 0; r < a.nranks; ++r) {
+            if (a.a_shards[r] == nullptr) return TGC_ERR_INVALID_ARG;
+            if (!aligned(a.a_shards[r], 16)) return TGC_ERR_ALIGN;
+        }
+    }
+    if (a.mode == TGC_MODE_FUSED) {
+        if (out.nblocks >= (int64_t(1) << 24)) return TGC_ERR_INVALID_ARG;
+        if (a.progress == nullptr || !aligned(a.progress, 4)) return TGC_ERR_INVALID_ARG;
+        if (a.workspace == nullptr) return TGC_ERR_WORKSPACE;
+        if (a.workspace_bytes < workspace_layout(out.nblocks).total) return TGC_ERR_WORKSPACE;
+        if (!aligned(a.workspace, 128)) return TGC_ERR_ALIGN;
+        if (a.order != nullptr) {
+            if (a.n_order < 0 || a.n_order > out.nblocks) return TGC_ERR_INVALID_ARG;
+            std::vector<char> seen((size_t)out.nblocks, 0);
+            for (int64_t i = 0; i < a.n_order; ++i) {
+                const int32_t c = a.order[i];
+                if (c < 0 || c >= out.nblocks || seen[(size_t)c]) return TGC_ERR_INVALID_ARG;
+                seen[(size_t)c] = 1;
+            }
+        }
+        // pieces per block * blocks must fit the 32-bit ticket dispenser
+        const int64_t pieces = (a.comm_block_rows * a.K * 2 + 8191) / 8192;
+        if (pieces * out.nblocks >= (int64_t(1) << 31)) return TGC_ERR_INVALID_ARG;
+    }
+    if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;
+    return 0;
+}
+
+static int ag_ex_impl(const tgc_ag_matmul_args &a) {
+    AGCheck chk{};
+    int rc = ag_validate(a, chk);
+    if (rc < 0) return rc;
+    if (rc == 1) return TGC_OK;  // empty problem
+    cudaError_t e;
+    cudaStream_t st = a.stream;
+    const uint64_t timeout = a.spin_timeout_ns ? a.spin_timeout_ns : 2000000000ull;
+
+    int32_t *status = a.d_status;
+    WorkspaceLayout wl = workspace_layout(chk.nblocks);
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    if (status == nullptr && ws != nullptr) status = reinterpret_cast<int32_t *>(ws + wl.status_off);
+    if (a.d_status != nullptr) {
+        e = cudaMemsetAsync(a.d_status, 0, sizeof(int32_t), st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+
+    GemmLaunch G{};
+    G.nranks = a.nranks;
+    G.B = a.B;
+    G.C = a.C;
+    G.a = a.a_out;
+    G.M = a.M;
+    G.K = a.K;
+    G.N = a.N;
+    G.cb = a.comm_block_rows;
+    G.rank = a.rank;
+    G.pivot = (int)a.pivot;
+    G.group_m = a.group_m > 0 ? a.group_m : 8;
+    G.grid = a.grid;
+    G.timeout_ns = timeout;
+    G.status = status;
+    if (a.mode != TGC_MODE_MM_ONLY)
+        for (int r = 0; r < a.nranks; ++r) G.shards[r] = a.a_shards[r];
+
+    if (a.mode == TGC_MODE_FUSED) {
+        G.fused = true;
+        G.progress = a.progress;
+        G.epoch = a.epoch;
+        G.ws_counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
+        G.ws_tickets = reinterpret_cast<uint32_t *>(ws + wl.tickets_off);
+        G.n_order = chk.nblocks;
+        if (a.order != nullptr) {
+            e = cudaMemcpyAsync(ws + wl.order_off, a.order, (size_t)a.n_order * 4, cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            G.order = reinterpret_cast<const int32_t *>(ws + wl.order_off);
+            G.n_order = a.n_order;
+        }
+        if (a.delay_ns != nullptr) {
+            e = cudaMemcpyAsync(ws + wl.delay_off, a.delay_ns, (size_t)chk.nblocks * 4, cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            G.delay_ns = reinterpret_cast<const uint32_t *>(ws + wl.delay_off);
+        }
+        if (status == nullptr) return TGC_ERR_WORKSPACE;
+        rc = launch_gemm(G, st);
+        if (rc != TGC_OK) return rc;
+    } else {
+        if (a.mode == TGC_MODE_UNFUSED) {
+            TGatherLaunch T{};
+            for (int r = 0; r < a.nranks; ++r) T.srcs[r] = a.a_shards[r];
+            T.dst = a.a_out;
+            T.nranks = a.nranks;
+            T.es = 2;
+            T.nslab = 1;
+            T.run_bytes = chk.rows_per_rank * a.K * 2;
+            T.dst_slab_bytes = a.M * a.K * 2;
+            T.seg_bytes = T.run_bytes;
+            T.nseg = 1;
+            if (T.run_bytes > 0) {
+                rc = launch_tgather(T, st);
+                if (rc != TGC_OK) return rc;
+            }
+        }
+        G.fused = false;
+        rc = launch_gemm(G, st);
+        if (rc != TGC_OK) return rc;
+    }
+
+    if (a.sync) {
+        if (status == nullptr) {
+            e = cudaStreamSynchronize(st);
+            return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+        }
+        int32_t h = 0;
+        e = cudaMemcpyAsync(&h, status, sizeof h, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return h;
+    }
+    return TGC_OK;
+}
+
+}  // namespace tgc
+
+using namespace tgc;
+
+extern "C" {
+
+int tgc_tgather(void *dst, const void *const *srcs, int nranks, int64_t D0, int64_t D1, int64_t D2, int64_t H,
+                int64_t W, tgc_dtype dtype, cudaStream_t stream) {
+    tgc_tgather_args a{};
+    a.dst = dst;
+    a.srcs = srcs;
+    a.nranks = nranks;
+    a.D0 = D0;
+    a.D1 = D1;
+    a.D2 = D2;
+    a.H = H;
+    a.W = W;
+    a.dtype = dtype;
+    a.stream = stream;
+    return tgather_impl(a);
+}
+
+int tgc_tgather_ex(const tgc_tgather_args *args) {
+    if (args == nullptr) return TGC_ERR_INVALID_ARG;
+    return tgather_impl(*args);
+}
+
+size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N, int64_t comm_block_rows) {
+    (void)K;
+    (void)N;
+    int64_t nblocks = 0;
+    if (nranks > 0 && comm_block_rows > 0 && M > 0) nblocks = M / comm_block_rows;
+    return workspace_layout(nblocks).total;
+}
+
+int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args) {
+    if (args == nullptr) return TGC_ERR_INVALID_ARG;
+    return ag_ex_impl(*args);
+}
+
+int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *C, int64_t M, int64_t K, int64_t N,
+                  int64_t comm_block_rows, cudaStream_t stream) {
+    tgc_ag_matmul_args a{};
+    a.a_shards = a_shards;
+    a.nranks = nranks;
+    a.B = B;
+    a.C = C;
+    a.M = M;
+    a.K = K;
+    a.N = N;
+    a.comm_block_rows = comm_block_rows;
+    a.mode = TGC_MODE_FUSED;
+    a.pivot = TGC_PIVOT_PAGE;
+    a.epoch = 1;
+    a.stream = stream;
+    a.sync = 1;
+    // validate with placeholder temporaries before allocating anything
+    {
+        tgc_ag_matmul_args probe = a;
+        alignas(256) static const uint64_t fake[64] = {0};
+        probe.a_out = const_cast<uint64_t *>(fake);
+        probe.progress = reinterpret_cast<uint32_t *>(const_cast<uint64_t *>(fake));
+        probe.workspace = const_cast<uint64_t *>(fake);
+        probe.workspace_bytes = (size_t)-1;
+        AGCheck chk{};
+        int rc = ag_validate(probe, chk);
+        if (rc < 0) return rc;
+        if (rc == 1) return TGC_OK;
+    }
+    const int64_t nblocks = M / comm_block_rows;
+    const size_t a_bytes = (size_t)M * (size_t)K * 2;
+    const size_t p_bytes = (size_t)nblocks * 4;
+    const size_t w_bytes = workspace_layout(nblocks).total;
+    void *d_a = nullptr, *d_p = nullptr, *d_w = nullptr;
+    int dev = 0;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = library_pool(dev, &pool);
+    if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&d_a, a_bytes, pool, stream);
+    if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&d_p, p_bytes, pool, stream);
+    if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&d_w, w_bytes, pool, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_p, 0, p_bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_w, 0, w_bytes, stream);
+    int rc = TGC_OK;
+    if (e != cudaSuccess) {
+        rc = cuda_fail(e);
+    } else {
+        a.a_out = d_a;
+        a.progress = static_cast<uint32_t *>(d_p);
+        a.workspace = d_w;
+        a.workspace_bytes = w_bytes;
+        rc = ag_ex_impl(a);  // synchronizes and returns the device status
+    }
+    if (d_a) cudaFreeAsync(d_a, stream);
+    if (d_p) cudaFreeAsync(d_p, stream);
+    if (d_w) cudaFreeAsync(d_w, stream);
+    e = cudaStreamSynchronize(stream);
+    if (rc == TGC_OK && e != cudaSuccess) rc = cuda_fail(e);
+    return rc;
+}
+
+int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks, int rank,
+                               tgc_pivot pivot, int group_m, int grid, int cta, int64_t *out, int64_t max_tiles) {
+    if (M <= 0 || N <= 0 || nranks <= 0 || M % nranks != 0 || rank < 0 || rank >= nranks || grid <= 0 ||
+        cta < 0 || cta >= grid || group_m < 0 || comm_block_rows <= 0)
+        return TGC_ERR_INVALID_ARG;
+    if (pivot != TGC_PIVOT_PAGE && pivot != TGC_PIVOT_SHARD && pivot != TGC_PIVOT_NONE) return TGC_ERR_INVALID_ARG;
+    TileSchedule s{};
+    s.num_pid_m = (int)((M + kBM - 1) / kBM);
+    s.num_pid_n = (int)((N + kBN - 1) / kBN);
+    s.num_tiles = s.num_pid_m * s.num_pid_n;
+    s.group_m = group_m > 0 ? group_m : 8;
+    s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kBM, s.num_pid_m);
+    int64_t n = 0;
+    for (int t = cta; t < s.num_tiles; t += grid, ++n) {
+        if (out != nullptr && n < max_tiles) {
+            int pm, pn;
+            s.tile(t, pm, pn);
+            out[2 * n] = pm;
+            out[2 * n + 1] = pn;
+        }
+    }
+    return n;
+}
+
+void tgc_gemm_tile_shape(int *bm, int *bn, int *bk) {
+    if (bm) *bm = kBM;
+    if (bn) *bn = kBN;
+    if (bk) *bk = kBK;
+}
+
+const char *tgc_status_string(int status) {
+    switch (status) {
+        case TGC_OK: return "ok";
+        case TGC_ERR_INVALID_ARG: return "invalid argument";
+        case TGC_ERR_DTYPE: return "unsupported dtype";
+        case TGC_ERR_ALIGN: return "misaligned pointer or row pitch";
+        case TGC_ERR_NOT_RESIDENT: return "persistent grid cannot be made resident";
+        case TGC_ERR_CUDA: return "CUDA error (see tgc_last_cuda_error)";
+        case TGC_ERR_TIMEOUT: return "bounded device wait expired";
+        case TGC_ERR_ABORTED: return "kernel aborted after another CTA failed";
+        case TGC_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int tgc_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *tgc_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,490 @@
+// gemm.cu -- persistent, warp-specialised bf16 GEMM C = a * B^T on tcgen05 /
+// TMEM / TMA for sm_103a, in two variants:
+//   FUSED = true : the AllGather is produced inside the kernel.  Producer
+//                  warps copy communication blocks of the shards into `a` and
+//                  publish progress[block] = epoch; tiles that need remote
+//                  rows wait on exactly the blocks they cover.
+//   FUSED = false: plain GEMM over `a` (the unfused path's second kernel and
+//                  the "mm_only" ceiling).
+//
+// Source: "Triton第四课：基于对称内存融合 AllGather 与 MatMul，提速1.56倍":
+//   融合后的流水线 -- tiles pivoted by rank; a tile whose comm block belongs to
+//       the caller reads a_shard directly, any other tile waits for
+//       progress[comm_block_id] and reads the aggregate buffer a;
+//   数据搬运与细粒度同步 -- progress entry src_rank*splits_per_rank+split_id
+//       is set once the block's data is in place; data before flag;
+//   wait_signal 的实现与语义 -- one thread polls the flag, then the CTA
+//       proceeds; here one warp polls (one lane per covered block) with
+//       ld.acquire.gpu and the wait is bounded.
+//
+// CTA anatomy (256 threads, one CTA per SM, persistent over tiles):
+//   warp 0     scheduler + flag wait + TMA loads of A (128x64) and B (256x64)
+//              tiles into a 4-stage shared-memory ring (128-byte swizzle)
+//   warp 1     TMEM owner; one lane issues tcgen05.mma 128x256x16 into one of
+//              two TMEM accumulators (2 x 256 fp32 columns)
+//   warp 2     (FUSED) copy producer: bulk async copies global -> shared ->
+//              global of 8 KiB pieces of comm blocks, pieces handed out by a
+//              global ticket so any resident CTA can copy any block; the last
+//              piece of a block publishes its flag
+//   warps 4..7 epilogue: tcgen05.ld of the accumulator (one TMEM lane quarter
+//              per warp), fp32 -> bf16 round-to-nearest-even, stores to C
+// The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
+// tile i+1.  All waits are bounded; on expiry the kernel records a status,
+// lets its in-flight copies and MMAs land, frees TMEM and returns.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "prims.cuh"
+#include "schedule.h"
+
+namespace tgc {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kAStage = kBM * kBK * 2;  // 16 KiB
+constexpr int kBStage = kBN * kBK * 2;  // 32 KiB
+constexpr int kSlots = 4;
+constexpr int kSlotBytes = 8192;
+constexpr uint32_t kTmemCols = 512;     // two 128x256 fp32 accumulators
+constexpr uint32_t kIdesc = make_idesc_bf16_f32(kBM, kBN);
+constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
+
+constexpr int smem_bytes(bool fused) {
+    return 1024 /* alignment slack */ + kStages * (kAStage + kBStage) + (fused ? kSlots * kSlotBytes : 0) +
+           256 /* barriers + TMEM address */;
+}
+
+struct GemmParams {
+    int M, N, K;
+    int num_kb;
+    TileSchedule sched;
+    uint16_t *C;
+    int *status;
+    uint64_t timeout_ns;       // flag waits
+    uint64_t mbar_timeout_ns;  // pipeline waits
+    // fused-only
+    int cb;
+    int nblocks;
+    int blocks_per_rank;
+    int rows_per_rank;
+    int local_row0, local_row1;
+    int local_b0, local_b1;
+    int first_block;
+    int n_order;
+    int pieces_per_block;
+    int64_t row_bytes;
+    int64_t block_bytes;
+    const uint8_t *shards[TGC_MAX_RANKS];
+    uint8_t *a;
+    uint32_t *progress;
+    uint32_t epoch;
+    const int32_t *order;      // device copy in the workspace, or null
+    const uint32_t *delay_ns;  // device copy in the workspace, or null
+    uint32_t *counters;
+    uint32_t *tickets;
+};
+
+// ---------------------------------------------------------------- flag wait
+
+// Warp-collective: wait until progress[b] == epoch for every b in [b0, b1].
+// Lane i polls block b0 + i (+32, ...) with gpu-scope acquire loads.
+__device__ bool wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
+    for (int base = b0; base <= b1; base += 32) {
+        const int b = base + lane;
+        const bool need = b <= b1;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint64_t iter = 0;; ++iter) {
+            const bool ready = !need || ld_acquire_gpu(p.progress + b) == p.epoch;
+            if (__all_sync(0xffffffffu, ready)) break;
+            if ((iter & 7) == 7) {
+                const bool bad = ld_status(p.status) != 0;
+                bool late = (globaltimer_ns() - t0 > p.timeout_ns) || iter > (1ull << 36);
+                late = __shfl_sync(0xffffffffu, late, 0);
+                if (late && lane == 0) raise_status(p.status, kStatusTimeout);
+                if (__any_sync(0xffffffffu, bad || late)) return false;
+            }
+            __nanosleep(32);
+        }
+    }
+    __syncwarp();
+    fence_proxy_async_global();  // the TMA loads that follow read what the flags published
+    return true;
+}
+
+// ---------------------------------------------------------------- roles
+
+template <bool FUSED>
+__device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
+                         const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
+                         int lane) {
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.sched.num_tiles; t += gridDim.x) {
+        int pid_m, pid_n;
+        p.sched.tile(t, pid_m, pid_n);
+        const int m0 = pid_m * kBM, n0 = pid_n * kBN;
+        const CUtensorMap *mapA = tmA;
+        int arow = m0;
+        if (FUSED) {
+            if (m0 >= p.local_row0 && m0 + kBM <= p.local_row1) {
+                mapA = tmL;               // rows of the caller's own shard: no wait
+                arow = m0 - p.local_row0;
+            } else {
+                const int m1 = (m0 + kBM) < p.M ? (m0 + kBM) : p.M;
+                if (!wait_blocks(p, m0 / p.cb, (m1 - 1) / p.cb, lane)) { ok = false; break; }
+            }
+        }
+        if (lane == 0) {
+            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+                mbar_arrive_expect_tx(&full[s], kAStage + kBStage);
+                tma_load_2d(sA + s * kAStage, mapA, &full[s], kb * kBK, arow);
+                tma_load_2d(sB + s * kBStage, tmB, &full[s], kb * kBK, n0);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+        // let every issued stage land before shared memory is given up
+        for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+            const uint32_t n_s = it / kStages + (s < it % kStages ? 1u : 0u);
+            if (n_s > 0) mbar_drain_wait(&full[s], (n_s - 1) & 1u, kDrainTimeoutNs);
+        }
+    }
+    __syncwarp();
+}
+
+__device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
+                         uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, int lane) {
+    if (lane == 0) {
+        uint32_t it = 0, tc = 0;
+        bool ok = true;
+        const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
+        for (int t = blockIdx.x; t < p.sched.num_tiles && ok; t += gridDim.x, ++tc) {
+            const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+            if (!mbar_wait(&tempty[acc], aph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem_base + acc * (uint32_t)kBN;
+            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!mbar_wait(&full[s], ph, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t ad = make_sw128_kmajor_desc(a_base + s * kAStage);
+                const uint64_t bd = make_sw128_kmajor_desc(b_base + s * kBStage);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                    mma_bf16_ss(d, ad + 2u * k, bd + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+            }
+            if (ok) mma_commit(&tfull[acc]);
+        }
+        mma_commit(drain);  // every MMA issued above has completed once this arrives
+        mbar_drain_wait(drain, 0, kDrainTimeoutNs);
+    }
+    __syncwarp();
+}
+
+__device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
+                              int warp, int lane) {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < p.sched.num_tiles; t += gridDim.x, ++tc) {
+        int pid_m, pid_n;
+        p.sched.tile(t, pid_m, pid_n);
+        const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&tfull[acc], aph, p.status, p.mbar_timeout_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform: tcgen05.ld is .sync.aligned
+        if (!ok) break;
+        tc_fence_after();
+        const int m = pid_m * kBM + row;
+        const int n0 = pid_n * kBN;
+        uint16_t *crow = p.C + (int64_t)m * p.N;
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)kBN;
+#pragma unroll 1
+        for (int j = 0; j < kBN / 32; ++j) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+            tmem_wait_ld();
+            if (m < p.M) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int n = n0 + j * 32 + c * 8;
+                    if (n < p.N) {
+                        uint4 o;
+                        o.x = pack_bf16x2(v[c * 8 + 0], v[c * 8 + 1]);
+                        o.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
+                        o.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
+                        o.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
+                        *reinterpret_cast<uint4 *>(crow + n) = o;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+    }
+}
+
+struct Piece {
+    const uint8_t *src;
+    uint8_t *dst;
+    uint32_t bytes;
+    int block;
+};
+
+__device__ __forceinline__ Piece piece_of(const GemmParams &p, uint32_t ticket) {
+    const int pos = (int)(ticket / (uint32_t)p.pieces_per_block);
+    const int j = (int)(ticket % (uint32_t)p.pieces_per_block);
+    const int c = p.order != nullptr
+                      ? p.order[pos]
+                      : default_release_block(pos, p.nblocks, p.first_block, p.local_b0, p.local_b1);
+    const int r = c / p.blocks_per_rank, s = c % p.blocks_per_rank;
+    const int64_t off = (int64_t)j * kSlotBytes;
+    const int64_t rem = p.block_bytes - off;
+    Piece pc;
+    pc.src = p.shards[r] + (int64_t)s * p.block_bytes + off;
+    pc.dst = p.a + ((int64_t)r * p.rows_per_rank + (int64_t)s * p.cb) * p.row_bytes + off;
+    pc.bytes = (uint32_t)(rem < kSlotBytes ? rem : kSlotBytes);
+    pc.block = c;
+    return pc;
+}
+
+// A piece's bytes are globally written: count it; the block's last piece publishes the block.
+__device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticket) {
+    const Piece pc = piece_of(p, ticket);
+    const uint32_t old = atom_add_acq_rel_gpu(p.counters + pc.block, 1u);
+    if (old + 1 == (uint32_t)p.pieces_per_block) {
+        st_relaxed_gpu(p.counters + pc.block, 0u);  // every piece of this block is counted
+        if (p.delay_ns != nullptr) spin_for_ns(p.delay_ns[pc.block]);
+        st_release_gpu(p.progress + pc.block, p.epoch);
+    }
+}
+
+__device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar, int lane) {
+    if (lane != 0) return;
+    const uint32_t total = (uint32_t)p.n_order * (uint32_t)p.pieces_per_block;
+    uint32_t ring[kSlots];
+    uint32_t head = 0, tail = 0, ret = 0;  // stored / loaded / retired pieces of this CTA
+    bool nomore = false, ok = true;
+    for (;;) {
+        while (!nomore && tail - ret < (uint32_t)kSlots) {  // slot tail%kSlots is free: its piece retired
+            const uint32_t tk = atom_add_relaxed_gpu(p.tickets, 1u);
+            if (tk >= total) { nomore = true; break; }
+            const uint32_t slot = tail % kSlots;
+            ring[slot] = tk;
+            const Piece pc = piece_of(p, tk);
+            mbar_arrive_expect_tx(&slotbar[slot], pc.bytes);
+            bulk_g2s(sSlot + slot * kSlotBytes, pc.src, pc.bytes, &slotbar[slot]);
+            ++tail;
+        }
+        if (head == tail) break;  // nothing loaded that is not stored, and no tickets left
+        {
+            const uint32_t slot = head % kSlots;
+            if (!mbar_wait(&slotbar[slot], (head / kSlots) & 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+            fence_proxy_async_shared();
+            const Piece pc = piece_of(p, ring[slot]);
+            bulk_s2g(pc.dst, sSlot + slot * kSlotBytes, pc.bytes);
+            bulk_commit();
+            ++head;
+        }
+        bulk_wait<1>();  // every store but the newest has fully landed in global memory
+        if (ret + 1 < head) {
+            fence_proxy_async_global();
+            while (ret + 1 < head) { retire_piece(p, ring[ret % kSlots]); ++ret; }
+        }
+    }
+    bulk_wait<0>();
+    if (ok) {
+        fence_proxy_async_global();
+        while (ret < head) { retire_piece(p, ring[ret % kSlots]); ++ret; }
+        // the last producer to finish rewinds the ticket dispenser for the next call
+        const uint32_t done = atom_add_acq_rel_gpu(p.tickets + 1, 1u);
+        if (done + 1 == gridDim.x) {
+            st_relaxed_gpu(p.tickets, 0u);
+            st_relaxed_gpu(p.tickets + 1, 0u);
+        }
+    } else {
+        for (uint32_t i = head; i < tail; ++i) mbar_drain_wait(&slotbar[i % kSlots], (i / kSlots) & 1u, kDrainTimeoutNs);
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <bool FUSED>
+__global__ void __launch_bounds__(kThreads, 1)
+    ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
+                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kStages * kAStage;
+    uint8_t *sSlot = sB + kStages * kBStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (FUSED ? kSlots * kSlotBytes : 0));
+    uint64_t *full = bars;
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *slotbar = tempty + 2;
+    uint64_t *drain = slotbar + kSlots;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        for (int i = 0; i < kSlots; ++i) mbar_init(&slotbar[i], 1);
+        mbar_init(drain, 1);
+        fence_mbarrier_init();
+        fence_proxy_async_shared();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        if (FUSED) prefetch_tensormap(&tmL);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        role_tma<FUSED>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, lane);
+    } else if (warp == 1) {
+        role_mma(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, lane);
+    } else if (warp == 2) {
+        if (FUSED) role_copy(p, sSlot, slotbar, lane);
+    } else if (warp >= 4) {
+        role_epilogue(p, tfull, tempty, tmem_base, warp, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D bf16 row-major (rows x cols) with a (box_rows x 64) box, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool FUSED>
+static int set_smem_attr() {
+    static cudaError_t err = cudaErrorUnknown;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(ag_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_bytes(FUSED));
+    });
+    return err == cudaSuccess ? TGC_OK : cuda_fail(err);
+}
+
+int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.M = (int)L.M;
+    p.N = (int)L.N;
+    p.K = (int)L.K;
+    p.num_kb = (int)((L.K + kBK - 1) / kBK);
+    p.sched.num_pid_m = (int)((L.M + kBM - 1) / kBM);
+    p.sched.num_pid_n = (int)((L.N + kBN - 1) / kBN);
+    p.sched.num_tiles = p.sched.num_pid_m * p.sched.num_pid_n;
+    p.sched.group_m = L.group_m;
+    const int64_t rows_per_rank = L.M / L.nranks;
+    p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, kBM, p.sched.num_pid_m);
+    p.C = static_cast<uint16_t *>(L.C);
+    p.status = L.status;
+    p.timeout_ns = L.timeout_ns;
+    p.mbar_timeout_ns = 4 * L.timeout_ns + 100ull * 1000 * 1000;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int sms = sm_count(dev);
+
+    CUtensorMap tmA, tmL, tmB;
+    if (!make_map(&tmA, L.a, L.M, L.K, kBM) || !make_map(&tmB, L.B, L.N, L.K, kBN)) return TGC_ERR_CUDA;
+    if (L.fused) {
+        if (!make_map(&tmL, L.shards[L.rank], rows_per_rank, L.K, kBM)) return TGC_ERR_CUDA;
+        p.cb = (int)L.cb;
+        p.nblocks = (int)(L.M / L.cb);
+        p.blocks_per_rank = (int)(rows_per_rank / L.cb);
+        p.rows_per_rank = (int)rows_per_rank;
+        p.local_row0 = (int)(L.rank * rows_per_rank);
+        p.local_row1 = (int)((L.rank + 1) * rows_per_rank);
+        p.local_b0 = L.rank * p.blocks_per_rank;
+        p.local_b1 = (L.rank + 1) * p.blocks_per_rank;
+        p.first_block = (int)(((int64_t)p.sched.pivot_off * kBM) / L.cb);
+        p.n_order = (int)L.n_order;
+        p.row_bytes = L.K * 2;
+        p.block_bytes = L.cb * L.K * 2;
+        p.pieces_per_block = (int)((p.block_bytes + kSlotBytes - 1) / kSlotBytes);
+        for (int r = 0; r < L.nranks; ++r) p.shards[r] = static_cast<const uint8_t *>(L.shards[r]);
+        p.a = static_cast<uint8_t *>(L.a);
+        p.progress = L.progress;
+        p.epoch = L.epoch;
+        p.order = L.order;
+        p.delay_ns = L.delay_ns;
+        p.counters = L.ws_counters;
+        p.tickets = L.ws_tickets;
+    } else {
+        tmL = tmA;
+    }
+
+    int grid = L.grid > 0 ? L.grid : sms;
+    if (!L.fused && grid > p.sched.num_tiles) grid = p.sched.num_tiles;
+    if (grid < 1) grid = 1;
+
+    int rc = L.fused ? set_smem_attr<true>() : set_smem_attr<false>();
+    if (rc != TGC_OK) return rc;
+    if (L.fused)
+        ag_gemm_kernel<true><<<grid, kThreads, smem_bytes(true), stream>>>(tmA, tmL, tmB, p);
+    else
+        ag_gemm_kernel<false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmL, tmB, p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+}
+
+}  // namespace tgc

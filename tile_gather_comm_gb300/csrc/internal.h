@@ -1,0 +1,70 @@
+// internal.h -- host-side declarations shared by the translation units of
+// libtgc.so (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tgc.h"
+
+namespace tgc {
+
+constexpr int kBM = 128;   // GEMM tile rows (tcgen05 M)
+constexpr int kBN = 256;   // GEMM tile cols (tcgen05 N)
+constexpr int kBK = 64;    // bf16 elements per 128-byte swizzled row
+
+// Records a CUDA error for tgc_last_cuda_error() and maps it to a status.
+int cuda_fail(cudaError_t e);
+int sm_count(int device);
+
+// Launch the TGATHER kernel; arguments already validated.
+struct TGatherLaunch {
+    const void *srcs[TGC_MAX_RANKS];
+    void *dst;
+    int nranks;
+    int64_t nslab, run_bytes, dst_slab_bytes, seg_bytes, nseg;
+    int es;
+    uint32_t *progress;
+    uint32_t *counters;
+    uint32_t epoch;
+};
+int launch_tgather(const TGatherLaunch &L, cudaStream_t stream);
+
+// Launch one of the GEMM kernels; arguments already validated.
+struct GemmLaunch {
+    bool fused;
+    const void *shards[TGC_MAX_RANKS];
+    int nranks;
+    const void *B;
+    void *C;
+    void *a;           // gathered A (written by the fused producer, read by tiles)
+    int64_t M, K, N;
+    int64_t cb;        // comm_block_rows
+    int rank;
+    int pivot;
+    int group_m;
+    int grid;
+    uint32_t *progress;
+    uint32_t epoch;
+    const int32_t *order;
+    int64_t n_order;
+    const uint32_t *delay_ns;
+    uint64_t timeout_ns;
+    uint32_t *ws_counters;  // nblocks
+    uint32_t *ws_tickets;   // [0] piece ticket, [1] finished producers
+    int32_t *status;
+};
+int launch_gemm(const GemmLaunch &L, cudaStream_t stream);
+
+// Workspace layout of tgc_ag_matmul_ex.
+struct WorkspaceLayout {
+    size_t status_off;    // int32 status word
+    size_t tickets_off;   // 2 x uint32
+    size_t counters_off;  // nblocks x uint32 piece counters
+    size_t order_off;     // nblocks x int32: device copy of the release order
+    size_t delay_off;     // nblocks x uint32: device copy of the release delays
+    size_t total;
+};
+WorkspaceLayout workspace_layout(int64_t nblocks);
+
+}  // namespace tgc

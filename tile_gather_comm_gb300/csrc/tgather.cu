@@ -1,0 +1,202 @@
+// tgather.cu -- TGATHER row-concatenation gather for sm_103a.
+//
+// Source: "CANN PTO-ISA TGATHER 指令深度解析：跨 Rank 行拼接 Gather 的实现原理与开发指南"
+//   §二 数学语义: dst[d0,d1,d2, r*H+i, j] = src^(r)[d0,d1,d2,i,j].
+//   §6.1: the NPU version stages tiles through its unified buffer with a 2-D
+//   sliding window and masks for ragged tiles.
+//
+// GPU design.  With dense tensors, the H*W elements of rank r in slab
+// (d0,d1,d2) are ONE contiguous run in the source and ONE contiguous run in
+// the destination, so the whole gather is nranks*D0*D1*D2 contiguous copies.
+// Each run is cut into segments (one per progress chunk, or the whole run),
+// each segment into tiles of TILE_VECS vectors; a persistent grid walks the
+// (segment, tile) items.  Copies go through registers with VW-byte vectors
+// (16 bytes whenever the source and destination agree modulo 16), coalesced:
+// consecutive threads touch consecutive vectors.  The unaligned head and the
+// ragged tail of a segment (fewer than VW bytes each) are copied element by
+// element by the segment's first tile -- this replaces the page's dynamic
+// ValidRow/ValidCol masks, so any H and W work.
+//
+// Per-chunk release: when progress is given, the CTA that finishes the last
+// tile of chunk (r, s) -- counted with an acq_rel atomic -- stores `epoch`
+// into progress[r*S + s] with st.release.gpu ("Triton第四课：基于对称内存融合
+// AllGather 与 MatMul，提速1.56倍", section 数据搬运与细粒度同步: data visible
+// before the flag).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "prims.cuh"
+
+namespace tgc {
+
+constexpr int kTGThreads = 256;
+constexpr int kTGUnroll = 4;
+
+struct TGParams {
+    const uint8_t *srcs[TGC_MAX_RANKS];
+    uint8_t *dst;
+    int nranks;
+    int es;
+    int64_t nslab;
+    int64_t run_bytes;       // H*W*es: one (rank, slab) run; also the source slab stride
+    int64_t dst_slab_bytes;  // dst_rows3*W*es
+    int64_t seg_bytes;       // bytes per segment (chunk_rows*W*es, or run_bytes)
+    int64_t nseg;            // segments per run
+    int64_t tiles_per_seg;   // upper bound, identical for every segment
+    int64_t total_items;
+    uint32_t *progress;
+    uint32_t *counters;
+    uint32_t epoch;
+};
+
+template <int VW> struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8> { using T = uint2; };
+template <> struct VecT<4> { using T = uint32_t; };
+template <> struct VecT<2> { using T = uint16_t; };
+template <> struct VecT<1> { using T = uint8_t; };
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+template <typename T>
+__device__ __forceinline__ T ld_stream(const T *p) { return __ldg(p); }
+
+// Element-wise copy of `n` bytes (n and both addresses multiples of es).
+__device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t n, int es, int tid, int nt) {
+    switch (es) {
+        case 8: for (int64_t i = tid; i < n / 8; i += nt) reinterpret_cast<uint64_t *>(d)[i] = reinterpret_cast<const uint64_t *>(s)[i]; break;
+        case 4: for (int64_t i = tid; i < n / 4; i += nt) reinterpret_cast<uint32_t *>(d)[i] = reinterpret_cast<const uint32_t *>(s)[i]; break;
+        case 2: for (int64_t i = tid; i < n / 2; i += nt) reinterpret_cast<uint16_t *>(d)[i] = reinterpret_cast<const uint16_t *>(s)[i]; break;
+        default: for (int64_t i = tid; i < n; i += nt) d[i] = s[i]; break;
+    }
+}
+
+template <int VW>
+__global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
+    using V = typename VecT<VW>::T;
+    constexpr int64_t kTileVecs = (int64_t)kTGThreads * kTGUnroll;
+    const int tid = threadIdx.x;
+
+    for (int64_t item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+        // item = ((s * nranks + r) * nslab + slab) * tiles_per_seg + tile
+        const int64_t tile = item % p.tiles_per_seg;
+        int64_t rest = item / p.tiles_per_seg;
+        const int64_t slab = rest % p.nslab;
+        rest /= p.nslab;
+        const int r = (int)(rest % p.nranks);
+        const int64_t s = rest / p.nranks;
+
+        const int64_t seg_off = s * p.seg_bytes;
+        const int64_t len0 = p.run_bytes - seg_off;
+        const int64_t len = len0 < p.seg_bytes ? len0 : p.seg_bytes;
+        const uint8_t *src = p.srcs[r] + slab * p.run_bytes + seg_off;
+        uint8_t *dst = p.dst + slab * p.dst_slab_bytes + (int64_t)r * p.run_bytes + seg_off;
+
+        // Split [0, len) into head (to VW alignment of src), vector body, tail.
+        int64_t head = (int64_t)((VW - (reinterpret_cast<uintptr_t>(src) % VW)) % VW);
+        if (head > len) head = len;
+        const int64_t nvec = (len - head) / VW;
+        const int64_t body_end = head + nvec * VW;
+
+        const int64_t v0 = tile * kTileVecs;
+        if (v0 < nvec) {
+            const V *vs = reinterpret_cast<const V *>(src + head) + v0;
+            V *vd = reinterpret_cast<V *>(dst + head) + v0;
+            const int64_t n = (nvec - v0) < kTileVecs ? (nvec - v0) : kTileVecs;
+            V reg[kTGUnroll];
+#pragma unroll
+            for (int k = 0; k < kTGUnroll; ++k) {
+                const int64_t idx = tid + (int64_t)k * kTGThreads;
+                if (idx < n) reg[k] = ld_stream(vs + idx);
+            }
+#pragma unroll
+            for (int k = 0; k < kTGUnroll; ++k) {
+                const int64_t idx = tid + (int64_t)k * kTGThreads;
+                if (idx < n) vd[idx] = reg[k];
+            }
+        }
+        if (tile == 0) {
+            if (head > 0) copy_elems(dst, src, head, p.es, tid, kTGThreads);
+            if (len > body_end) copy_elems(dst + body_end, src + body_end, len - body_end, p.es, tid, kTGThreads);
+        }
+
+        if (p.progress != nullptr) {
+            // Publish chunk (r, s) once all its nslab*tiles_per_seg items are written.
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const int64_t c = (int64_t)r * p.nseg + s;
+                const uint32_t target = (uint32_t)(p.nslab * p.tiles_per_seg);
+                const uint32_t old = atom_add_acq_rel_gpu(p.counters + c, 1u);
+                if (old + 1 == target) {
+                    st_relaxed_gpu(p.counters + c, 0u);  // no other item of this chunk remains
+                    st_release_gpu(p.progress + c, p.epoch);
+                }
+            }
+        }
+    }
+}
+
+static int pick_vw(const TGatherLaunch &L) {
+    // Largest power of two <= 16 dividing every (src - dst) address difference;
+    // then source and destination share their alignment modulo VW everywhere.
+    uint64_t g = 16;
+    const uint64_t slab_delta = (uint64_t)(L.dst_slab_bytes - L.run_bytes);
+    auto fold = [&](uint64_t x) {
+        while (g > 1 && (x % g) != 0) g >>= 1;
+    };
+    for (int r = 0; r < L.nranks; ++r) {
+        const uint64_t d = reinterpret_cast<uintptr_t>(L.dst) + (uint64_t)r * (uint64_t)L.run_bytes;
+        fold(reinterpret_cast<uintptr_t>(L.srcs[r]) - d);
+    }
+    if (L.nslab > 1) fold(slab_delta);
+    if ((int)g < L.es) g = (uint64_t)L.es;  // cannot happen for element-aligned pointers
+    return (int)g;
+}
+
+int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
+    TGParams p{};
+    for (int r = 0; r < L.nranks; ++r) p.srcs[r] = static_cast<const uint8_t *>(L.srcs[r]);
+    p.dst = static_cast<uint8_t *>(L.dst);
+    p.nranks = L.nranks;
+    p.es = L.es;
+    p.nslab = L.nslab;
+    p.run_bytes = L.run_bytes;
+    p.dst_slab_bytes = L.dst_slab_bytes;
+    p.seg_bytes = L.seg_bytes;
+    p.nseg = L.nseg;
+    p.progress = L.progress;
+    p.counters = L.counters;
+    p.epoch = L.epoch;
+
+    const int vw = pick_vw(L);
+    const int64_t tile_bytes = (int64_t)kTGThreads * kTGUnroll * vw;
+    const int64_t max_vecs = L.seg_bytes / vw;
+    p.tiles_per_seg = max_vecs > 0 ? (max_vecs + (tile_bytes / vw) - 1) / (tile_bytes / vw) : 1;
+    if (p.tiles_per_seg < 1) p.tiles_per_seg = 1;
+    p.total_items = L.nseg * (int64_t)L.nranks * L.nslab * p.tiles_per_seg;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t slots = (int64_t)sm_count(dev) * (2048 / kTGThreads);
+    const int64_t waves = (p.total_items + slots - 1) / slots;
+    const int64_t grid = (p.total_items + waves - 1) / waves;
+
+    switch (vw) {
+        case 16: tgather_kernel<16><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+        case 8: tgather_kernel<8><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+        case 4: tgather_kernel<4><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+        case 2: tgather_kernel<2><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+        default: tgather_kernel<1><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+    }
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+}
+
+}  // namespace tgc
