@@ -1,0 +1,67 @@
+"""bench.py's multi-rank host logic on CPU (gloo, world_size 2): barrier and
+max-over-ranks timing, whole-job throughput = units of all ranks / max time,
+and the reference arm running on rank 0 only."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist()
+    d.barrier()
+    value, ms = bench.aggregate(10.0 * (rank + 1), 1e12, d)   # rank 1 is the slow one: 20 ms
+    q.put((rank, value, ms, d.max(rank)))
+    d.close()
+
+
+def test_aggregate_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, value, ms, mx in out:
+        assert ms == 20.0                      # max over ranks
+        assert abs(value - 100.0) < 1e-9       # 2 ranks x 1e12 flop / 20 ms = 100 TFLOP/s
+        assert mx == 1
+
+
+def _run_bench(rank):
+    env = dict(os.environ, WORLD_SIZE="2", RANK=str(rank), LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+               MASTER_PORT=str(_free_port()))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                           "tiny", "--steps", "2", "--warmup", "1"], env=env, capture_output=True, text=True,
+                          timeout=300)
+
+
+def test_reference_arm_prints_on_rank0_only():
+    r1 = _run_bench(1)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = _run_bench(0)
+    assert r0.returncode == 0
+    lines = [l for l in r0.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
