@@ -215,6 +215,12 @@ typedef enum tgc_pivot {
  *                NULL the status word lives in the workspace (FUSED) or is
  *                not kept (UNFUSED / MM_ONLY without workspace).
  *   sync         nonzero: synchronize `stream` and return the device status.
+ *   trace        optional device uint64 array of grid*TGC_TRACE_WORDS words
+ *                (grid = the persistent CTA count actually launched, at most
+ *                the SM count): per CTA, %globaltimer stamps and signal-wait
+ *                totals, laid out as the TGC_TRACE_* indices below.  NULL
+ *                records nothing.  The page's evaluation advice asks for the
+ *                time spent waiting on signals to be reported separately.
  * Calls that share a workspace or progress array must not overlap on the GPU.
  */
 typedef struct tgc_ag_matmul_args {
@@ -241,9 +247,21 @@ typedef struct tgc_ag_matmul_args {
     int32_t *d_status;
     int sync;
     cudaStream_t stream;
+    uint64_t *trace;
 } tgc_ag_matmul_args;
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
+
+/* Per-CTA trace words (all times in ns of %globaltimer). */
+#define TGC_TRACE_WORDS 8
+#define TGC_TRACE_START 0       /* CTA start                                   */
+#define TGC_TRACE_WAIT_NS 1     /* total time the tile scheduler spent on flags */
+#define TGC_TRACE_WAITED_TILES 2 /* tiles that found a flag not yet set         */
+#define TGC_TRACE_COPY_FIRST 3  /* producer: first piece handed out            */
+#define TGC_TRACE_COPY_LAST 4   /* producer: last piece of this CTA retired    */
+#define TGC_TRACE_PIECES 5      /* producer: pieces copied by this CTA         */
+#define TGC_TRACE_END 6         /* epilogue: last tile of this CTA stored      */
+#define TGC_TRACE_TILES 7       /* tiles computed by this CTA                  */
 
 /* Bytes of workspace tgc_ag_matmul_ex needs for this problem (>= 256). */
 size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N,

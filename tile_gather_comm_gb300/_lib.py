@@ -31,6 +31,8 @@ DTYPES = {
     torch.int32: 4, torch.float32: 5, torch.int64: 6, torch.float64: 7,
 }
 MAX_RANKS = 64
+TRACE_WORDS = 8
+TRACE = dict(start=0, wait_ns=1, waited_tiles=2, copy_first=3, copy_last=4, pieces=5, end=6, tiles=7)
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -57,7 +59,7 @@ class AgMatmulArgs(ctypes.Structure):
         ("delay_ns", ctypes.POINTER(ctypes.c_uint32)),
         ("spin_timeout_ns", ctypes.c_uint64), ("group_m", ctypes.c_int), ("grid", ctypes.c_int),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("d_status", _vp),
-        ("sync", ctypes.c_int), ("stream", _vp),
+        ("sync", ctypes.c_int), ("stream", _vp), ("trace", _vp),
     ]
 
 
@@ -192,7 +194,7 @@ def tgc_ag_matmul_workspace_bytes(nranks: int, M: int, K: int, N: int, comm_bloc
 def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | None = None, rank: int = 0,
                      mode: str = "fused", pivot: str = "page", progress=None, epoch: int = 1, order=None,
                      delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, grid: int = 0,
-                     workspace=None, d_status=None, sync: bool = False, stream=None,
+                     workspace=None, d_status=None, sync: bool = False, stream=None, trace=None,
                      check: bool = True) -> int:
     """Extended AllGather-MatMul (see tgc.h).  ``order`` / ``delay_ns`` are host sequences."""
     R = len(a_shards) if a_shards is not None else 1
@@ -216,7 +218,7 @@ def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | No
         progress=_ptr(progress), epoch=epoch, order=order_arr, n_order=n_order, delay_ns=delay_arr,
         spin_timeout_ns=spin_timeout_ns, group_m=group_m, grid=grid, workspace=_ptr(workspace),
         workspace_bytes=(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
-        d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream))
+        d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream), trace=_ptr(trace))
     rc = lib().tgc_ag_matmul_ex(ctypes.byref(a))
     return _check(rc, "tgc_ag_matmul_ex") if check else rc
 

@@ -188,6 +188,7 @@ static int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
         if (pieces * out.nblocks >= (int64_t(1) << 31)) return TGC_ERR_INVALID_ARG;
     }
     if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;
+    if (a.trace != nullptr && !aligned(a.trace, 8)) return TGC_ERR_ALIGN;
     return 0;
 }
 
@@ -224,6 +225,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.grid = a.grid;
     G.timeout_ns = timeout;
     G.status = status;
+    G.trace = a.trace;
     if (a.mode != TGC_MODE_MM_ONLY)
         for (int r = 0; r < a.nranks; ++r) G.shards[r] = a.a_shards[r];
 

@@ -50,7 +50,8 @@ constexpr int kThreads = 256;
 constexpr int kAStage = kBM * kBK * 2;  // 16 KiB
 constexpr int kBStage = kBN * kBK * 2;  // 32 KiB
 constexpr int kSlots = 4;
-constexpr int kSlotBytes = 8192;
+constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
+constexpr int kPieceBytes = 65536;      // unit of the ticket dispenser and of block completion
 constexpr uint32_t kTmemCols = 512;     // two 128x256 fp32 accumulators
 constexpr uint32_t kIdesc = make_idesc_bf16_f32(kBM, kBN);
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
@@ -88,13 +89,21 @@ struct GemmParams {
     const uint32_t *delay_ns;  // device copy in the workspace, or null
     uint32_t *counters;
     uint32_t *tickets;
+    uint64_t *trace;  // optional: kTraceWords per CTA
 };
+
+// Trace word indices (mirrors TGC_TRACE_* in tgc.h).
+constexpr int kTraceWords = 8;
+enum : int { kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles };
 
 // ---------------------------------------------------------------- flag wait
 
 // Warp-collective: wait until progress[b] == epoch for every b in [b0, b1].
 // Lane i polls block b0 + i (+32, ...) with gpu-scope acquire loads.
-__device__ bool wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
+// Returns -1 if the wait was abandoned (timeout or abort), 0 if every flag was
+// already set at the first poll, 1 if the warp had to spin.
+__device__ int wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
+    int waited = 0;
     for (int base = b0; base <= b1; base += 32) {
         const int b = base + lane;
         const bool need = b <= b1;
@@ -102,19 +111,20 @@ __device__ bool wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
         for (uint64_t iter = 0;; ++iter) {
             const bool ready = !need || ld_acquire_gpu(p.progress + b) == p.epoch;
             if (__all_sync(0xffffffffu, ready)) break;
+            waited = 1;
             if ((iter & 7) == 7) {
                 const bool bad = ld_status(p.status) != 0;
                 bool late = (globaltimer_ns() - t0 > p.timeout_ns) || iter > (1ull << 36);
                 late = __shfl_sync(0xffffffffu, late, 0);
                 if (late && lane == 0) raise_status(p.status, kStatusTimeout);
-                if (__any_sync(0xffffffffu, bad || late)) return false;
+                if (__any_sync(0xffffffffu, bad || late)) return -1;
             }
             __nanosleep(32);
         }
     }
     __syncwarp();
     fence_proxy_async_global();  // the TMA loads that follow read what the flags published
-    return true;
+    return waited;
 }
 
 // ---------------------------------------------------------------- roles
@@ -125,6 +135,7 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
                          int lane) {
     uint32_t it = 0;
     bool ok = true;
+    uint64_t wait_ns = 0, waited_tiles = 0;
     for (int t = blockIdx.x; t < p.sched.num_tiles; t += gridDim.x) {
         int pid_m, pid_n;
         p.sched.tile(t, pid_m, pid_n);
@@ -137,7 +148,13 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
                 arow = m0 - p.local_row0;
             } else {
                 const int m1 = (m0 + kBM) < p.M ? (m0 + kBM) : p.M;
-                if (!wait_blocks(p, m0 / p.cb, (m1 - 1) / p.cb, lane)) { ok = false; break; }
+                const uint64_t w0 = p.trace != nullptr ? globaltimer_ns() : 0;
+                const int w = wait_blocks(p, m0 / p.cb, (m1 - 1) / p.cb, lane);
+                if (w < 0) { ok = false; break; }
+                if (p.trace != nullptr && w > 0) {
+                    wait_ns += globaltimer_ns() - w0;
+                    ++waited_tiles;
+                }
             }
         }
         if (lane == 0) {
@@ -151,6 +168,10 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
+    }
+    if (p.trace != nullptr && lane == 0) {
+        p.trace[blockIdx.x * kTraceWords + kTrWaitNs] = wait_ns;
+        p.trace[blockIdx.x * kTraceWords + kTrWaitedTiles] = waited_tiles;
     }
     if (!ok && lane == 0) {
         // let every issued stage land before shared memory is given up
@@ -233,6 +254,10 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
     }
+    if (p.trace != nullptr && warp == 4 && lane == 0) {
+        p.trace[blockIdx.x * kTraceWords + kTrEnd] = globaltimer_ns();
+        p.trace[blockIdx.x * kTraceWords + kTrTiles] = tc;
+    }
 }
 
 struct Piece {
@@ -249,12 +274,12 @@ __device__ __forceinline__ Piece piece_of(const GemmParams &p, uint32_t ticket) 
                       ? p.order[pos]
                       : default_release_block(pos, p.nblocks, p.first_block, p.local_b0, p.local_b1);
     const int r = c / p.blocks_per_rank, s = c % p.blocks_per_rank;
-    const int64_t off = (int64_t)j * kSlotBytes;
+    const int64_t off = (int64_t)j * kPieceBytes;
     const int64_t rem = p.block_bytes - off;
     Piece pc;
     pc.src = p.shards[r] + (int64_t)s * p.block_bytes + off;
     pc.dst = p.a + ((int64_t)r * p.rows_per_rank + (int64_t)s * p.cb) * p.row_bytes + off;
-    pc.bytes = (uint32_t)(rem < kSlotBytes ? rem : kSlotBytes);
+    pc.bytes = (uint32_t)(rem < kPieceBytes ? rem : kPieceBytes);
     pc.block = c;
     return pc;
 }
@@ -270,43 +295,105 @@ __device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticke
     }
 }
 
+// Copy producer (one lane).  Work arrives in pieces of up to kPieceBytes,
+// handed out by a global ticket (any resident CTA can copy any block), and
+// flows through kSlots shared-memory slots as sub-copies of up to kSlotBytes:
+// bulk load global -> slot, then bulk store slot -> `a`.  A slot is reused as
+// soon as its store has finished READING shared memory, while the store's
+// global writes may still be in flight.  A piece is retired -- counted toward
+// its block, and the block published by the piece that completes it -- once
+// the writes of its last sub-copy have landed, which may lag up to kStoreLag
+// stores behind, so loads, stores in flight and retirement overlap.
+constexpr int kStoreLag = 6;
+constexpr int kPieceRing = 16;  // pieces loaded but not yet retired (> kStoreLag + kSlots)
+
 __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar, int lane) {
     if (lane != 0) return;
     const uint32_t total = (uint32_t)p.n_order * (uint32_t)p.pieces_per_block;
-    uint32_t ring[kSlots];
-    uint32_t head = 0, tail = 0, ret = 0;  // stored / loaded / retired pieces of this CTA
-    bool nomore = false, ok = true;
+    // sub-copy sequence numbers: [0, tail) loads issued, [0, head) stores issued
+    uint32_t head = 0, tail = 0;
+    uint32_t slot_piece[kSlots];   // piece ring index of the sub-copy in each slot
+    uint32_t slot_off[kSlots];     // byte offset of that sub-copy within its piece
+    // piece ring: [pret, pload) pieces with sub-copies in flight or unretired
+    uint32_t ring_ticket[kPieceRing];
+    uint32_t ring_last_store[kPieceRing];  // store sequence number of the piece's last sub-copy (+1)
+    uint32_t pret = 0, pload = 0;
+    Piece cur{};
+    uint32_t cur_off = 0, cur_ring = 0;
+    bool have_cur = false, nomore = false, ok = true;
+    const uint64_t t_first = p.trace != nullptr ? globaltimer_ns() : 0;
     for (;;) {
-        while (!nomore && tail - ret < (uint32_t)kSlots) {  // slot tail%kSlots is free: its piece retired
-            const uint32_t tk = atom_add_relaxed_gpu(p.tickets, 1u);
-            if (tk >= total) { nomore = true; break; }
+        // issue loads while a slot is free (its previous store has read it)
+        while (tail - head < (uint32_t)kSlots) {
+            if (!have_cur) {
+                if (nomore || pload - pret >= (uint32_t)kPieceRing) break;
+                const uint32_t tk = atom_add_relaxed_gpu(p.tickets, 1u);
+                if (tk >= total) { nomore = true; break; }
+                cur = piece_of(p, tk);
+                cur_off = 0;
+                cur_ring = pload % kPieceRing;
+                ring_ticket[cur_ring] = tk;
+                ring_last_store[cur_ring] = 0;  // unknown yet
+                ++pload;
+                have_cur = true;
+            }
             const uint32_t slot = tail % kSlots;
-            ring[slot] = tk;
-            const Piece pc = piece_of(p, tk);
-            mbar_arrive_expect_tx(&slotbar[slot], pc.bytes);
-            bulk_g2s(sSlot + slot * kSlotBytes, pc.src, pc.bytes, &slotbar[slot]);
+            const uint32_t left = cur.bytes - cur_off;
+            const uint32_t nb = left < (uint32_t)kSlotBytes ? left : (uint32_t)kSlotBytes;
+            slot_piece[slot] = cur_ring;
+            slot_off[slot] = cur_off;
+            mbar_arrive_expect_tx(&slotbar[slot], nb);
+            bulk_g2s(sSlot + slot * kSlotBytes, cur.src + cur_off, nb, &slotbar[slot]);
+            cur_off += nb;
+            if (cur_off == cur.bytes) have_cur = false;
             ++tail;
         }
-        if (head == tail) break;  // nothing loaded that is not stored, and no tickets left
+        if (head == tail) {
+            if (nomore && !have_cur) break;
+            if (pload - pret >= (uint32_t)kPieceRing) {  // ring full: retire what has landed
+                bulk_wait<0>();
+                fence_proxy_async_global();
+                while (pret < pload && ring_last_store[pret % kPieceRing] != 0) {
+                    retire_piece(p, ring_ticket[pret % kPieceRing]);
+                    ++pret;
+                }
+            }
+            continue;
+        }
         {
             const uint32_t slot = head % kSlots;
             if (!mbar_wait(&slotbar[slot], (head / kSlots) & 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
             fence_proxy_async_shared();
-            const Piece pc = piece_of(p, ring[slot]);
-            bulk_s2g(pc.dst, sSlot + slot * kSlotBytes, pc.bytes);
+            const uint32_t pr = slot_piece[slot];
+            const Piece pc = piece_of(p, ring_ticket[pr]);
+            const uint32_t off = slot_off[slot];
+            const uint32_t left = pc.bytes - off;
+            const uint32_t nb = left < (uint32_t)kSlotBytes ? left : (uint32_t)kSlotBytes;
+            bulk_s2g(pc.dst + off, sSlot + slot * kSlotBytes, nb);
             bulk_commit();
             ++head;
+            if (off + nb == pc.bytes) ring_last_store[pr] = head;  // stores [0, head) cover this piece
         }
-        bulk_wait<1>();  // every store but the newest has fully landed in global memory
-        if (ret + 1 < head) {
-            fence_proxy_async_global();
-            while (ret + 1 < head) { retire_piece(p, ring[ret % kSlots]); ++ret; }
+        bulk_wait_read<0>();  // the store just issued has read its slot
+        // retire the oldest pieces whose last store is older than the newest kStoreLag
+        if (pret < pload) {
+            const uint32_t ls = ring_last_store[pret % kPieceRing];
+            if (ls != 0 && head - ls >= (uint32_t)kStoreLag) {
+                bulk_wait<kStoreLag>();  // all but the newest kStoreLag stores have landed
+                fence_proxy_async_global();
+                while (pret < pload) {
+                    const uint32_t l2 = ring_last_store[pret % kPieceRing];
+                    if (l2 == 0 || head - l2 < (uint32_t)kStoreLag) break;
+                    retire_piece(p, ring_ticket[pret % kPieceRing]);
+                    ++pret;
+                }
+            }
         }
     }
     bulk_wait<0>();
     if (ok) {
         fence_proxy_async_global();
-        while (ret < head) { retire_piece(p, ring[ret % kSlots]); ++ret; }
+        while (pret < pload) { retire_piece(p, ring_ticket[pret % kPieceRing]); ++pret; }
         // the last producer to finish rewinds the ticket dispenser for the next call
         const uint32_t done = atom_add_acq_rel_gpu(p.tickets + 1, 1u);
         if (done + 1 == gridDim.x) {
@@ -315,6 +402,11 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
         }
     } else {
         for (uint32_t i = head; i < tail; ++i) mbar_drain_wait(&slotbar[i % kSlots], (i / kSlots) & 1u, kDrainTimeoutNs);
+    }
+    if (p.trace != nullptr) {
+        p.trace[blockIdx.x * kTraceWords + kTrCopyFirst] = t_first;
+        p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = globaltimer_ns();
+        p.trace[blockIdx.x * kTraceWords + kTrPieces] = pret;
     }
 }
 
@@ -341,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        if (p.trace != nullptr) p.trace[blockIdx.x * kTraceWords + kTrStart] = globaltimer_ns();
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
         for (int i = 0; i < kSlots; ++i) mbar_init(&slotbar[i], 1);
@@ -438,6 +531,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     p.status = L.status;
     p.timeout_ns = L.timeout_ns;
     p.mbar_timeout_ns = 4 * L.timeout_ns + 100ull * 1000 * 1000;
+    p.trace = L.trace;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -460,7 +554,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.n_order = (int)L.n_order;
         p.row_bytes = L.K * 2;
         p.block_bytes = L.cb * L.K * 2;
-        p.pieces_per_block = (int)((p.block_bytes + kSlotBytes - 1) / kSlotBytes);
+        p.pieces_per_block = (int)((p.block_bytes + kPieceBytes - 1) / kPieceBytes);
         for (int r = 0; r < L.nranks; ++r) p.shards[r] = static_cast<const uint8_t *>(L.shards[r]);
         p.a = static_cast<uint8_t *>(L.a);
         p.progress = L.progress;

@@ -53,6 +53,7 @@ struct GemmLaunch {
     uint32_t *ws_counters;  // nblocks
     uint32_t *ws_tickets;   // [0] piece ticket, [1] finished producers
     int32_t *status;
+    uint64_t *trace;        // optional, kTraceWords per CTA
 };
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 

@@ -174,6 +174,13 @@ __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Wait until at most N bulk groups are still reading their shared-memory
+// source (the source may then be overwritten; the writes may still be in flight).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // 2-D tiled TMA load: box at (c0 = inner coordinate, c1 = outer) into smem.
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
     asm volatile(
