@@ -48,7 +48,8 @@ typedef enum tgc_status {
     TGC_ERR_CUDA = -5,         /* a CUDA call failed: see tgc_last_cuda_error */
     TGC_ERR_TIMEOUT = -6,      /* a bounded device wait expired               */
     TGC_ERR_ABORTED = -7,      /* the kernel stopped because another CTA timed out */
-    TGC_ERR_WORKSPACE = -8     /* workspace missing or too small              */
+    TGC_ERR_WORKSPACE = -8,    /* workspace missing or too small              */
+    TGC_ERR_TOO_LARGE = -9     /* problem exceeds tgc_ag_matmul_noalloc's fixed scratch */
 } tgc_status;
 
 /* Element types.  TGATHER only uses the element size ([TG] §7.1: source,
@@ -262,6 +263,36 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 #define TGC_TRACE_PIECES 5      /* producer: pieces copied by this CTA         */
 #define TGC_TRACE_END 6         /* epilogue: last tile of this CTA stored      */
 #define TGC_TRACE_TILES 7       /* tiles computed by this CTA                  */
+
+/*
+ * tgc_ag_matmul_noalloc -- the fused AllGather-MatMul of tgc_ag_matmul with
+ * no device allocation.  No counterpart on the pages: this is a library
+ * convenience for callers that cannot call cudaMalloc -- for instance code
+ * running under a memory manager that owns all device memory and forbids raw
+ * allocations, or a latency-critical path on which no allocation may happen
+ * after start-up.
+ *
+ * Arguments as in tgc_ag_matmul, plus
+ *   a_out   device (M, K) bf16 output: the gathered A (as in tgc_ag_matmul_ex).
+ * The scratch the fused kernel needs (status word, ticket dispenser, per-block
+ * counters and progress flags) lives in a fixed 64 KiB array of device memory
+ * declared statically in the library, one per GPU that loads the library and
+ * held until the process exits.  Limit: M / comm_block_rows <= 
+ * TGC_NOALLOC_MAX_BLOCKS comm blocks; larger problems return
+ * TGC_ERR_TOO_LARGE before anything is enqueued.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the same array, which keeps the previous
+ * call's contents: each call clears the part it uses (cudaMemsetAsync on
+ * `stream`) before launching.  Calls that overlap on the GPU -- on different
+ * streams or from different host threads -- race on the array and must not be
+ * issued.  Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Synchronizes `stream` and returns the device status, like tgc_ag_matmul.
+ */
+#define TGC_NOALLOC_MAX_BLOCKS 2048
+int tgc_ag_matmul_noalloc(const void *const *a_shards, int nranks, const void *B, void *C, void *a_out,
+                          int64_t M, int64_t K, int64_t N, int64_t comm_block_rows,
+                          cudaStream_t stream);
 
 /* Bytes of workspace tgc_ag_matmul_ex needs for this problem (>= 256). */
 size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N,

@@ -23,6 +23,8 @@ TGC_ERR_CUDA = -5
 TGC_ERR_TIMEOUT = -6
 TGC_ERR_ABORTED = -7
 TGC_ERR_WORKSPACE = -8
+TGC_ERR_TOO_LARGE = -9
+NOALLOC_MAX_BLOCKS = 2048
 
 MODES = {"fused": 0, "unfused": 1, "mm_only": 2}
 PIVOTS = {"page": 0, "shard": 1, "none": 2}
@@ -90,6 +92,9 @@ def lib() -> ctypes.CDLL:
     L.tgc_ag_matmul.restype = ctypes.c_int
     L.tgc_ag_matmul_ex.argtypes = [ctypes.POINTER(AgMatmulArgs)]
     L.tgc_ag_matmul_ex.restype = ctypes.c_int
+    L.tgc_ag_matmul_noalloc.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
+                                         _i64, _vp]
+    L.tgc_ag_matmul_noalloc.restype = ctypes.c_int
     L.tgc_ag_matmul_workspace_bytes.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64]
     L.tgc_ag_matmul_workspace_bytes.restype = ctypes.c_size_t
     L.tgc_ag_matmul_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -185,6 +190,18 @@ def tgc_ag_matmul(a_shards, B, C, comm_block_rows: int, stream=None, check: bool
     rc = lib().tgc_ag_matmul(_ptrs(a_shards), R, _ptr(B), _ptr(C), R * H, K, N, comm_block_rows,
                              _stream(stream))
     return _check(rc, "tgc_ag_matmul") if check else rc
+
+
+def tgc_ag_matmul_noalloc(a_shards, B, C, a_out, comm_block_rows: int, stream=None, check: bool = True) -> int:
+    """Fused AllGather-MatMul without any device allocation (for callers that cannot allocate):
+    the kernel's scratch is a fixed array inside the library; ``a_out`` receives the gathered A.
+    Synchronizes the stream."""
+    R = len(a_shards)
+    H, K = a_shards[0].shape
+    N = B.shape[0]
+    rc = lib().tgc_ag_matmul_noalloc(_ptrs(a_shards), R, _ptr(B), _ptr(C), _ptr(a_out), R * H, K, N,
+                                     comm_block_rows, _stream(stream))
+    return _check(rc, "tgc_ag_matmul_noalloc") if check else rc
 
 
 def tgc_ag_matmul_workspace_bytes(nranks: int, M: int, K: int, N: int, comm_block_rows: int) -> int:

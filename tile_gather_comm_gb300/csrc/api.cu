@@ -22,15 +22,17 @@ int cuda_fail(cudaError_t e) {
 }
 
 int sm_count(int device) {
+    constexpr int kMaxDevices = 64;
+    static int cache[kMaxDevices] = {0};
     static std::mutex mu;
-    static std::vector<int> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    if ((int)cache.size() <= device) cache.resize(device + 1, 0);
-    if (cache[device] == 0) {
+    auto query = [](int d) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 1;
-        cache[device] = n;
-    }
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 1;
+        return n;
+    };
+    if (device < 0 || device >= kMaxDevices) return query(device);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[device] == 0) cache[device] = query(device);
     return cache[device];
 }
 
@@ -131,12 +133,7 @@ static int tgather_impl(const tgc_tgather_args &a) {
 
 // ------------------------------------------------------------------ AG-MatMul
 
-struct AGCheck {
-    int64_t nblocks;
-    int64_t rows_per_rank;
-};
-
-static int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
+int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.nranks <= 0 || a.nranks > TGC_MAX_RANKS) return TGC_ERR_INVALID_ARG;
     if (a.M < 0 || a.K < 0 || a.N < 0) return TGC_ERR_INVALID_ARG;
     if (a.mode != TGC_MODE_FUSED && a.mode != TGC_MODE_UNFUSED && a.mode != TGC_MODE_MM_ONLY)
@@ -429,6 +426,7 @@ const char *tgc_status_string(int status) {
         case TGC_ERR_TIMEOUT: return "bounded device wait expired";
         case TGC_ERR_ABORTED: return "kernel aborted after another CTA failed";
         case TGC_ERR_WORKSPACE: return "workspace missing or too small";
+        case TGC_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of tgc_ag_matmul_noalloc";
         default: return "unknown status";
     }
 }

@@ -57,6 +57,14 @@ struct GemmLaunch {
 };
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 
+// Argument check shared by the AllGather-MatMul entry points: returns a
+// negative tgc_status, 0 when there is work, 1 when the problem is empty.
+struct AGCheck {
+    int64_t nblocks;
+    int64_t rows_per_rank;
+};
+int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out);
+
 // Workspace layout of tgc_ag_matmul_ex.
 struct WorkspaceLayout {
     size_t status_off;    // int32 status word
