@@ -205,7 +205,7 @@ typedef enum tgc_pivot {
  *                skew).
  *   spin_timeout_ns  limit for every device wait; 0 = 2 s.
  *   group_m      tile rows per swizzle group; 0 = default (8).
- *   grid         persistent CTAs; 0 = one per SM.
+ *   grid         persistent CTAs (used in pairs); 0 = every SM.
  *   workspace    device memory of tgc_ag_matmul_workspace_bytes() bytes,
  *                128-byte aligned, zero-filled once by the caller before first
  *                use; every call that succeeds leaves its counters and status
@@ -300,16 +300,18 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
 
 /*
  * Host-side copy of the tile schedule the GEMM kernels run (the same code the
- * device uses): writes, for persistent CTA `cta` of `grid`, the sequence of
- * (pid_m, pid_n) pairs it processes into out[2*t], out[2*t+1], at most
- * max_tiles pairs; returns the number of tiles of that CTA, or a negative
- * tgc_status.  Needs no GPU.
+ * device uses).  A tile is tgc_gemm_tile_shape()'s BM x BN outputs, computed
+ * by one persistent cluster (a pair of CTAs on two SMs).  Writes, for cluster
+ * `cta` of `grid` persistent clusters, the sequence of (pid_m, pid_n) pairs it
+ * processes into out[2*t], out[2*t+1], at most max_tiles pairs; returns the
+ * number of tiles of that cluster, or a negative tgc_status.  Needs no GPU.
  */
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks,
                                int rank, tgc_pivot pivot, int group_m, int grid, int cta,
                                int64_t *out, int64_t max_tiles);
 
-/* Tile shape used by the GEMM kernels (BM, BN, BK). */
+/* Tile shape used by the GEMM kernels (BM, BN, BK): BM rows are shared by a
+ * pair of CTAs (128 each), BK is the K depth of one pipeline stage. */
 void tgc_gemm_tile_shape(int *bm, int *bn, int *bk);
 
 /* ------------------------------------------------------------------------ */

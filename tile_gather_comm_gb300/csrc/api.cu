@@ -392,11 +392,11 @@ int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, in
         return TGC_ERR_INVALID_ARG;
     if (pivot != TGC_PIVOT_PAGE && pivot != TGC_PIVOT_SHARD && pivot != TGC_PIVOT_NONE) return TGC_ERR_INVALID_ARG;
     TileSchedule s{};
-    s.num_pid_m = (int)((M + kBM - 1) / kBM);
+    s.num_pid_m = (int)((M + kTileM - 1) / kTileM);
     s.num_pid_n = (int)((N + kBN - 1) / kBN);
     s.num_tiles = s.num_pid_m * s.num_pid_n;
     s.group_m = group_m > 0 ? group_m : 8;
-    s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kBM, s.num_pid_m);
+    s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kTileM, s.num_pid_m);
     int64_t n = 0;
     for (int t = cta; t < s.num_tiles; t += grid, ++n) {
         if (out != nullptr && n < max_tiles) {
@@ -410,7 +410,7 @@ int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, in
 }
 
 void tgc_gemm_tile_shape(int *bm, int *bn, int *bk) {
-    if (bm) *bm = kBM;
+    if (bm) *bm = kTileM;
     if (bn) *bn = kBN;
     if (bk) *bk = kBK;
 }

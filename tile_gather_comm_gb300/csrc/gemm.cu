@@ -17,11 +17,19 @@
 //       proceeds; here one warp polls (one lane per covered block) with
 //       ld.acquire.gpu and the wait is bounded.
 //
+// Tiles are 256 x 256 outputs computed by a CTA pair (a cluster of 2 CTAs on
+// two SMs, tcgen05 cta_group::2): each CTA holds 128 rows of A and 128 of the
+// 256 columns of B per stage, the even CTA issues the 256 x 256 x 16 MMAs for
+// both, and each CTA's TMEM receives its 128 rows of the accumulator.  A
+// single-CTA variant (128 x 256 tiles, cta_group::1) is kept behind the CG
+// template parameter.
+//
 // CTA anatomy (256 threads, one CTA per SM, persistent over tiles):
-//   warp 0     scheduler + flag wait + TMA loads of A (128x64) and B (256x64)
-//              tiles into a 4-stage shared-memory ring (128-byte swizzle)
-//   warp 1     TMEM owner; one lane issues tcgen05.mma 128x256x16 into one of
-//              two TMEM accumulators (2 x 256 fp32 columns)
+//   warp 0     scheduler + flag wait + TMA loads of this CTA's A (128x64) and
+//              B (128x64 per CTA of a pair, 256x64 alone) into a multi-stage
+//              shared-memory ring (128-byte swizzle)
+//   warp 1     TMEM owner; one lane (of the even CTA) issues tcgen05.mma into
+//              one of two TMEM accumulators (2 x 256 fp32 columns)
 //   warp 2     (FUSED) copy producer: bulk async copies global -> shared ->
 //              global of 8 KiB pieces of comm blocks, pieces handed out by a
 //              global ticket so any resident CTA can copy any block; the last
@@ -45,20 +53,31 @@
 
 namespace tgc {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 256;
-constexpr int kAStage = kBM * kBK * 2;  // 16 KiB
-constexpr int kBStage = kBN * kBK * 2;  // 32 KiB
 constexpr int kSlots = 4;
 constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
 constexpr int kPieceBytes = 65536;      // unit of the ticket dispenser and of block completion
-constexpr uint32_t kTmemCols = 512;     // two 128x256 fp32 accumulators
-constexpr uint32_t kIdesc = make_idesc_bf16_f32(kBM, kBN);
+constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns x 128 lanes
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 
+// Per-CTA-group configuration.  CG = number of CTAs sharing one MMA tile.
+template <int CG>
+struct Cfg {
+    static constexpr int kTileM = 128 * CG;             // output rows per (cluster) tile
+    static constexpr int kRowsCta = 128;                // rows of A per CTA
+    static constexpr int kHalfN = kBN / CG;             // rows of B (N) each CTA stages
+    static constexpr int kAStage = kRowsCta * kBK * 2;  // 16 KiB
+    static constexpr int kBStage = kHalfN * kBK * 2;    // 32 KiB alone, 16 KiB in a pair
+    static constexpr int kStages = CG == 1 ? 4 : 6;
+    static constexpr uint32_t kIdesc = make_idesc_bf16_f32(kTileM, kBN);
+    static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
+    static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
+};
+
+template <int CG>
 constexpr int smem_bytes(bool fused) {
-    return 1024 /* alignment slack */ + kStages * (kAStage + kBStage) + (fused ? kSlots * kSlotBytes : 0) +
-           256 /* barriers + TMEM address */;
+    return 1024 /* alignment slack */ + Cfg<CG>::kStages * (Cfg<CG>::kAStage + Cfg<CG>::kBStage) +
+           (fused ? kSlots * kSlotBytes : 0) + 256 /* barriers + TMEM address */;
 }
 
 struct GemmParams {
@@ -129,25 +148,36 @@ __device__ int wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
 
 // ---------------------------------------------------------------- roles
 
-template <bool FUSED>
+// Cluster-tile index space: cluster c of nclusters persistent clusters (a
+// "cluster" is a single CTA when CG == 1).
+template <int CG>
+__device__ __forceinline__ int cluster_id() { return (int)blockIdx.x / CG; }
+template <int CG>
+__device__ __forceinline__ int num_clusters() { return (int)gridDim.x / CG; }
+
+template <int CG, bool FUSED>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
-                         int lane) {
+                         uint32_t crank, int lane) {
+    using C = Cfg<CG>;
     uint32_t it = 0;
     bool ok = true;
     uint64_t wait_ns = 0, waited_tiles = 0;
-    for (int t = blockIdx.x; t < p.sched.num_tiles; t += gridDim.x) {
+    // completion of every stage is counted on the even CTA's full barrier
+    const uint32_t full0 = CG == 2 ? mapa_shared(smem_addr(full), 0) : smem_addr(full);
+    for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>()) {
         int pid_m, pid_n;
         p.sched.tile(t, pid_m, pid_n);
-        const int m0 = pid_m * kBM, n0 = pid_n * kBN;
+        const int m0 = pid_m * C::kTileM + (int)crank * C::kRowsCta;  // this CTA's 128 rows
+        const int nb = pid_n * kBN + (int)crank * C::kHalfN;          // this CTA's B rows
         const CUtensorMap *mapA = tmA;
         int arow = m0;
         if (FUSED) {
-            if (m0 >= p.local_row0 && m0 + kBM <= p.local_row1) {
+            if (m0 >= p.local_row0 && m0 + C::kRowsCta <= p.local_row1) {
                 mapA = tmL;               // rows of the caller's own shard: no wait
                 arow = m0 - p.local_row0;
-            } else {
-                const int m1 = (m0 + kBM) < p.M ? (m0 + kBM) : p.M;
+            } else if (m0 < p.M) {
+                const int m1 = (m0 + C::kRowsCta) < p.M ? (m0 + C::kRowsCta) : p.M;
                 const uint64_t w0 = p.trace != nullptr ? globaltimer_ns() : 0;
                 const int w = wait_blocks(p, m0 / p.cb, (m1 - 1) / p.cb, lane);
                 if (w < 0) { ok = false; break; }
@@ -159,11 +189,18 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         }
         if (lane == 0) {
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(&full[s], kAStage + kBStage);
-                tma_load_2d(sA + s * kAStage, mapA, &full[s], kb * kBK, arow);
-                tma_load_2d(sB + s * kBStage, tmB, &full[s], kb * kBK, n0);
+                if (CG == 1) {
+                    mbar_arrive_expect_tx(&full[s], C::kStageTx);
+                    tma_load_2d(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow);
+                    tma_load_2d(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb);
+                } else {
+                    if (crank == 0) mbar_arrive_expect_tx(&full[s], C::kStageTx);  // both CTAs' bytes
+                    const uint32_t bar = full0 + s * 8u;
+                    tma_load_2d_pair(sA + s * C::kAStage, mapA, bar, kb * kBK, arow);
+                    tma_load_2d_pair(sB + s * C::kBStage, tmB, bar, kb * kBK, nb);
+                }
             }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -174,51 +211,74 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         p.trace[blockIdx.x * kTraceWords + kTrWaitedTiles] = waited_tiles;
     }
     if (!ok && lane == 0) {
-        // let every issued stage land before shared memory is given up
-        for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
-            const uint32_t n_s = it / kStages + (s < it % kStages ? 1u : 0u);
-            if (n_s > 0) mbar_drain_wait(&full[s], (n_s - 1) & 1u, kDrainTimeoutNs);
+        if (CG == 1 || crank == 0) {
+            // let every stage this CTA expected land before shared memory is given up
+            for (uint32_t s = 0; s < (uint32_t)C::kStages; ++s) {
+                const uint32_t n_s = it / C::kStages + (s < it % C::kStages ? 1u : 0u);
+                if (n_s > 0) mbar_drain_wait(&full[s], (n_s - 1) & 1u, kDrainTimeoutNs);
+            }
+        } else {
+            // the odd CTA cannot observe the even CTA's barrier: give its own
+            // in-flight tile loads ample time to land
+            spin_for_ns(200000);
         }
     }
     __syncwarp();
 }
 
+template <int CG>
 __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
-                         uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, int lane) {
-    if (lane == 0) {
+                         uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, uint32_t crank,
+                         int lane) {
+    using C = Cfg<CG>;
+    if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
         const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
-        for (int t = blockIdx.x; t < p.sched.num_tiles && ok; t += gridDim.x, ++tc) {
+        for (int t = cluster_id<CG>(); t < p.sched.num_tiles && ok; t += num_clusters<CG>(), ++tc) {
             const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
             if (!mbar_wait(&tempty[acc], aph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + acc * (uint32_t)kBN;
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                 if (!mbar_wait(&full[s], ph, p.status, p.mbar_timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ad = make_sw128_kmajor_desc(a_base + s * kAStage);
-                const uint64_t bd = make_sw128_kmajor_desc(b_base + s * kBStage);
+                const uint64_t ad = make_sw128_kmajor_desc(a_base + s * C::kAStage);
+                const uint64_t bd = make_sw128_kmajor_desc(b_base + s * C::kBStage);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)
-                    mma_bf16_ss(d, ad + 2u * k, bd + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-                mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+                for (int k = 0; k < kBK / 16; ++k) {
+                    if (CG == 1)
+                        mma_bf16_ss(d, ad + 2u * k, bd + 2u * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    else
+                        mma_bf16_ss_pair(d, ad + 2u * k, bd + 2u * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+                }
+                // frees the stage (in both CTAs of a pair) once these MMAs have read it
+                if (CG == 1) mma_commit(&empty[s]);
+                else mma_commit_pair_mc(&empty[s], (uint16_t)0x3);
             }
-            if (ok) mma_commit(&tfull[acc]);
+            if (ok) {
+                if (CG == 1) mma_commit(&tfull[acc]);
+                else mma_commit_pair_mc(&tfull[acc], (uint16_t)0x3);
+            }
         }
-        mma_commit(drain);  // every MMA issued above has completed once this arrives
+        if (CG == 1) mma_commit(drain);  // every MMA issued above has completed once this arrives
+        else mma_commit_pair_mc(drain, (uint16_t)0x1);
         mbar_drain_wait(drain, 0, kDrainTimeoutNs);
     }
     __syncwarp();
 }
 
+template <int CG>
 __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
-                              int warp, int lane) {
+                              uint32_t crank, int warp, int lane) {
+    using C = Cfg<CG>;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    // the accumulator is released on the even CTA's barrier
+    const uint32_t tempty0 = CG == 2 ? mapa_shared(smem_addr(tempty), 0) : smem_addr(tempty);
     uint32_t tc = 0;
-    for (int t = blockIdx.x; t < p.sched.num_tiles; t += gridDim.x, ++tc) {
+    for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>(), ++tc) {
         int pid_m, pid_n;
         p.sched.tile(t, pid_m, pid_n);
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
@@ -227,7 +287,7 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform: tcgen05.ld is .sync.aligned
         if (!ok) break;
         tc_fence_after();
-        const int m = pid_m * kBM + row;
+        const int m = pid_m * C::kTileM + (int)crank * C::kRowsCta + row;
         const int n0 = pid_n * kBN;
         uint16_t *crow = p.C + (int64_t)m * p.N;
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)kBN;
@@ -252,7 +312,11 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
             }
         }
         tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        __syncwarp();
+        if (lane == 0) {
+            if (CG == 1) mbar_arrive(&tempty[acc]);
+            else mbar_arrive_cluster(tempty0 + acc * 8u);
+        }
     }
     if (p.trace != nullptr && warp == 4 && lane == 0) {
         p.trace[blockIdx.x * kTraceWords + kTrEnd] = globaltimer_ns();
@@ -412,30 +476,32 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
 
 // ---------------------------------------------------------------- kernel
 
-template <bool FUSED>
+template <int CG, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    using C = Cfg<CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *sA = smem;
-    uint8_t *sB = smem + kStages * kAStage;
-    uint8_t *sSlot = sB + kStages * kBStage;
+    uint8_t *sB = smem + C::kStages * C::kAStage;
+    uint8_t *sSlot = sB + C::kStages * C::kBStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (FUSED ? kSlots * kSlotBytes : 0));
     uint64_t *full = bars;
-    uint64_t *empty = full + kStages;
-    uint64_t *tfull = empty + kStages;
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *slotbar = tempty + 2;
     uint64_t *drain = slotbar + kSlots;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
         if (p.trace != nullptr) p.trace[blockIdx.x * kTraceWords + kTrStart] = globaltimer_ns();
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], C::kEpiArrivals); }
         for (int i = 0; i < kSlots; ++i) mbar_init(&slotbar[i], 1);
         mbar_init(drain, 1);
         fence_mbarrier_init();
@@ -447,29 +513,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (FUSED) prefetch_tensormap(&tmL);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
-        tmem_relinquish();
+        if (CG == 1) { tmem_alloc(tmem_holder, kTmemCols); tmem_relinquish(); }
+        else { tmem_alloc_pair(tmem_holder, kTmemCols); tmem_relinquish_pair(); }
     }
     tc_fence_before();
-    __syncthreads();
+    if (CG == 1) __syncthreads(); else cluster_sync();  // barriers initialised in both CTAs before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        role_tma<FUSED>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, lane);
+        role_tma<CG, FUSED>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
-        role_mma(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, lane);
+        role_mma<CG>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
     } else if (warp == 2) {
         if (FUSED) role_copy(p, sSlot, slotbar, lane);
     } else if (warp >= 4) {
-        role_epilogue(p, tfull, tempty, tmem_base, warp, lane);
+        role_epilogue<CG>(p, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
+    // In a pair, the even CTA's MMAs read the odd CTA's shared memory and write
+    // its TMEM, and its commits arrive on the odd CTA's barriers: neither CTA
+    // leaves (or frees TMEM) before both are done.
+    __syncwarp();  // reconverge each warp before the aligned barrier
     tc_fence_before();
-    __syncthreads();
+    if (CG == 1) __syncthreads(); else cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (CG == 1) tmem_dealloc(tmem_base, kTmemCols);
+        else tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -503,30 +574,82 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t col
     return r == CUDA_SUCCESS;
 }
 
-template <bool FUSED>
+// CTAs that share one MMA tile in the launched kernels.
+constexpr int kCG = 2;
+
+template <int CG, bool FUSED>
 static int set_smem_attr() {
     static cudaError_t err = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(ag_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes(FUSED));
+        err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_bytes<CG>(FUSED));
     });
     return err == cudaSuccess ? TGC_OK : cuda_fail(err);
 }
 
+// Persistent clusters that can be resident at once (one CTA per SM).
+template <int CG, bool FUSED>
+static int max_clusters(int sms) {
+    if (CG == 1) return sms;
+    static int cached = 0;
+    static std::once_flag once;
+    std::call_once(once, [sms] {
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CG;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes<CG>(FUSED);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED>, &cfg) != cudaSuccess || n <= 0)
+            n = sms / CG;
+        cached = n;
+    });
+    return cached;
+}
+
+template <int CG, bool FUSED>
+static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const GemmParams &p,
+                  int nclusters, cudaStream_t stream) {
+    int rc = set_smem_attr<CG, FUSED>();
+    if (rc != TGC_OK) return rc;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<CG>(FUSED);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED>, tmA, tmL, tmB, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+}
+
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
+    using C = Cfg<kCG>;
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     p.M = (int)L.M;
     p.N = (int)L.N;
     p.K = (int)L.K;
     p.num_kb = (int)((L.K + kBK - 1) / kBK);
-    p.sched.num_pid_m = (int)((L.M + kBM - 1) / kBM);
+    p.sched.num_pid_m = (int)((L.M + C::kTileM - 1) / C::kTileM);
     p.sched.num_pid_n = (int)((L.N + kBN - 1) / kBN);
     p.sched.num_tiles = p.sched.num_pid_m * p.sched.num_pid_n;
     p.sched.group_m = L.group_m;
     const int64_t rows_per_rank = L.M / L.nranks;
-    p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, kBM, p.sched.num_pid_m);
+    p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, C::kTileM, p.sched.num_pid_m);
     p.C = static_cast<uint16_t *>(L.C);
     p.status = L.status;
     p.timeout_ns = L.timeout_ns;
@@ -539,9 +662,10 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     const int sms = sm_count(dev);
 
     CUtensorMap tmA, tmL, tmB;
-    if (!make_map(&tmA, L.a, L.M, L.K, kBM) || !make_map(&tmB, L.B, L.N, L.K, kBN)) return TGC_ERR_CUDA;
+    if (!make_map(&tmA, L.a, L.M, L.K, C::kRowsCta) || !make_map(&tmB, L.B, L.N, L.K, C::kHalfN))
+        return TGC_ERR_CUDA;
     if (L.fused) {
-        if (!make_map(&tmL, L.shards[L.rank], rows_per_rank, L.K, kBM)) return TGC_ERR_CUDA;
+        if (!make_map(&tmL, L.shards[L.rank], rows_per_rank, L.K, C::kRowsCta)) return TGC_ERR_CUDA;
         p.cb = (int)L.cb;
         p.nblocks = (int)(L.M / L.cb);
         p.blocks_per_rank = (int)(rows_per_rank / L.cb);
@@ -550,7 +674,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.local_row1 = (int)((L.rank + 1) * rows_per_rank);
         p.local_b0 = L.rank * p.blocks_per_rank;
         p.local_b1 = (L.rank + 1) * p.blocks_per_rank;
-        p.first_block = (int)(((int64_t)p.sched.pivot_off * kBM) / L.cb);
+        p.first_block = (int)(((int64_t)p.sched.pivot_off * C::kTileM) / L.cb);
         p.n_order = (int)L.n_order;
         p.row_bytes = L.K * 2;
         p.block_bytes = L.cb * L.K * 2;
@@ -567,18 +691,16 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         tmL = tmA;
     }
 
-    int grid = L.grid > 0 ? L.grid : sms;
-    if (!L.fused && grid > p.sched.num_tiles) grid = p.sched.num_tiles;
-    if (grid < 1) grid = 1;
-
-    int rc = L.fused ? set_smem_attr<true>() : set_smem_attr<false>();
+    // persistent clusters: every SM busy; for the plain GEMM no more clusters than tiles
+    // (the shared-memory attribute must be set before the occupancy query)
+    int rc = L.fused ? set_smem_attr<kCG, true>() : set_smem_attr<kCG, false>();
     if (rc != TGC_OK) return rc;
-    if (L.fused)
-        ag_gemm_kernel<true><<<grid, kThreads, smem_bytes(true), stream>>>(tmA, tmL, tmB, p);
-    else
-        ag_gemm_kernel<false><<<grid, kThreads, smem_bytes(false), stream>>>(tmA, tmL, tmB, p);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+    int nclusters = L.fused ? max_clusters<kCG, true>(sms) : max_clusters<kCG, false>(sms);
+    if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
+    if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
+    if (nclusters < 1) nclusters = 1;
+    return L.fused ? launch<kCG, true>(tmA, tmL, tmB, p, nclusters, stream)
+                   : launch<kCG, false>(tmA, tmL, tmB, p, nclusters, stream);
 }
 
 }  // namespace tgc

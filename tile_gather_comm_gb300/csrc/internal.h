@@ -9,9 +9,9 @@
 
 namespace tgc {
 
-constexpr int kBM = 128;   // GEMM tile rows (tcgen05 M)
-constexpr int kBN = 256;   // GEMM tile cols (tcgen05 N)
-constexpr int kBK = 64;    // bf16 elements per 128-byte swizzled row
+constexpr int kBN = 256;     // GEMM tile cols (tcgen05 N)
+constexpr int kBK = 64;      // bf16 elements per 128-byte swizzled row
+constexpr int kTileM = 256;  // GEMM tile rows: a pair of CTAs, 128 rows each (tcgen05 cta_group::2)
 
 // Records a CUDA error for tgc_last_cuda_error() and maps it to a status.
 int cuda_fail(cudaError_t e);
