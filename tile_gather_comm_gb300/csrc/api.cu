@@ -218,7 +218,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.cb = a.comm_block_rows;
     G.rank = a.rank;
     G.pivot = (int)a.pivot;
-    G.group_m = a.group_m > 0 ? a.group_m : 8;
+    G.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
     G.grid = a.grid;
     G.timeout_ns = timeout;
     G.status = status;
@@ -395,7 +395,7 @@ int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, in
     s.num_pid_m = (int)((M + kTileM - 1) / kTileM);
     s.num_pid_n = (int)((N + kBN - 1) / kBN);
     s.num_tiles = s.num_pid_m * s.num_pid_n;
-    s.group_m = group_m > 0 ? group_m : 8;
+    s.group_m = group_m > 0 ? group_m : TGC_DEFAULT_GROUP_M;
     s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kTileM, s.num_pid_m);
     int64_t n = 0;
     for (int t = cta; t < s.num_tiles; t += grid, ++n) {

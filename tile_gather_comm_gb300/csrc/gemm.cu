@@ -53,32 +53,44 @@
 
 namespace tgc {
 
+// Compile-time tuning (defaults chosen by measurement on GB300).
+#ifndef TGC_PAIR_STAGES
+#define TGC_PAIR_STAGES 6        // pipeline stages of the plain GEMM on CTA pairs
+#endif
+#ifndef TGC_PAIR_FUSED_STAGES
+#define TGC_PAIR_FUSED_STAGES 6  // pipeline stages when the copy producer also needs shared memory
+#endif
+#ifndef TGC_COPY_SLOTS
+#define TGC_COPY_SLOTS 4         // staging slots of the copy producer
+#endif
+
 constexpr int kThreads = 256;
-constexpr int kSlots = 4;
+constexpr int kSlots = TGC_COPY_SLOTS;
 constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
 constexpr int kPieceBytes = 65536;      // unit of the ticket dispenser and of block completion
 constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns x 128 lanes
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 
 // Per-CTA-group configuration.  CG = number of CTAs sharing one MMA tile.
-template <int CG>
+template <int CG, bool FUSED>
 struct Cfg {
     static constexpr int kTileM = 128 * CG;             // output rows per (cluster) tile
     static constexpr int kRowsCta = 128;                // rows of A per CTA
     static constexpr int kHalfN = kBN / CG;             // rows of B (N) each CTA stages
     static constexpr int kAStage = kRowsCta * kBK * 2;  // 16 KiB
     static constexpr int kBStage = kHalfN * kBK * 2;    // 32 KiB alone, 16 KiB in a pair
-    static constexpr int kStages = CG == 1 ? 4 : 6;
+    static constexpr int kStages = CG == 1 ? 4 : (FUSED ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
     static constexpr uint32_t kIdesc = make_idesc_bf16_f32(kTileM, kBN);
     static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
     static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
 };
 
-template <int CG>
-constexpr int smem_bytes(bool fused) {
-    return 1024 /* alignment slack */ + Cfg<CG>::kStages * (Cfg<CG>::kAStage + Cfg<CG>::kBStage) +
-           (fused ? kSlots * kSlotBytes : 0) + 256 /* barriers + TMEM address */;
+template <int CG, bool FUSED>
+constexpr int smem_bytes() {
+    return 1024 /* alignment slack */ + Cfg<CG, FUSED>::kStages * (Cfg<CG, FUSED>::kAStage + Cfg<CG, FUSED>::kBStage) +
+           (FUSED ? kSlots * kSlotBytes : 0) + 256 /* barriers + TMEM address */;
 }
+static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<2, false>() <= 232448, "shared memory per CTA");
 
 struct GemmParams {
     int M, N, K;
@@ -159,7 +171,7 @@ template <int CG, bool FUSED>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint32_t crank, int lane) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, FUSED>;
     uint32_t it = 0;
     bool ok = true;
     uint64_t wait_ns = 0, waited_tiles = 0;
@@ -226,11 +238,11 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     __syncwarp();
 }
 
-template <int CG>
+template <int CG, bool FUSED>
 __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, uint32_t crank,
                          int lane) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, FUSED>;
     if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
@@ -269,10 +281,10 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
     __syncwarp();
 }
 
-template <int CG>
+template <int CG, bool FUSED>
 __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                               uint32_t crank, int warp, int lane) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, FUSED>;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     // the accumulator is released on the even CTA's barrier
@@ -480,7 +492,7 @@ template <int CG, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -524,11 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         role_tma<CG, FUSED>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
-        role_mma<CG>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
+        role_mma<CG, FUSED>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
     } else if (warp == 2) {
         if (FUSED) role_copy(p, sSlot, slotbar, lane);
     } else if (warp >= 4) {
-        role_epilogue<CG>(p, tfull, tempty, tmem_base, crank, warp, lane);
+        role_epilogue<CG, FUSED>(p, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
     // In a pair, the even CTA's MMAs read the odd CTA's shared memory and write
@@ -583,7 +595,7 @@ static int set_smem_attr() {
     static std::once_flag once;
     std::call_once(once, [] {
         err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes<CG>(FUSED));
+                                   smem_bytes<CG, FUSED>());
     });
     return err == cudaSuccess ? TGC_OK : cuda_fail(err);
 }
@@ -603,7 +615,7 @@ static int max_clusters(int sms) {
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes<CG>(FUSED);
+        cfg.dynamicSmemBytes = smem_bytes<CG, FUSED>();
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
@@ -627,7 +639,7 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CG>(FUSED);
+    cfg.dynamicSmemBytes = smem_bytes<CG, FUSED>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -637,7 +649,7 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
 }
 
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
-    using C = Cfg<kCG>;
+    using C = Cfg<kCG, false>;  // tile geometry does not depend on FUSED
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     p.M = (int)L.M;

@@ -7,6 +7,10 @@
 
 #include "../../include/tgc.h"
 
+#ifndef TGC_DEFAULT_GROUP_M
+#define TGC_DEFAULT_GROUP_M 8  // tile rows per swizzle group when the caller passes 0
+#endif
+
 namespace tgc {
 
 constexpr int kBN = 256;     // GEMM tile cols (tcgen05 N)
