@@ -170,12 +170,20 @@ typedef enum tgc_mode {
  *   SHARD: pid_m = (pid_m + floor(rank*(M/nranks) / BM)) % num_pid_m, which
  *          starts every rank on its own shard;
  *   NONE : no rotation.
- * The pivot only reorders tiles; C does not depend on it.
+ *   READY_QUEUE (FUSED only; the other modes treat it as NONE): the tile rows
+ *          lying entirely inside the caller's shard come first (they wait for
+ *          nothing); every other tile row is handed out in the order in which
+ *          its data becomes complete -- the producer that completes a tile row
+ *          appends it to a device ring, and the i-th position after the local
+ *          prefix takes the i-th row appended ([AGM] section 融合后的流水线:
+ *          tiles are processed "in their ready order").
+ * The order only changes which tile runs when; C does not depend on it.
  */
 typedef enum tgc_pivot {
     TGC_PIVOT_PAGE = 0,
     TGC_PIVOT_SHARD = 1,
-    TGC_PIVOT_NONE = 2
+    TGC_PIVOT_NONE = 2,
+    TGC_PIVOT_READY_QUEUE = 3
 } tgc_pivot;
 
 /*
@@ -305,6 +313,7 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
  * `cta` of `grid` persistent clusters, the sequence of (pid_m, pid_n) pairs it
  * processes into out[2*t], out[2*t+1], at most max_tiles pairs; returns the
  * number of tiles of that cluster, or a negative tgc_status.  Needs no GPU.
+ * READY_QUEUE has no static order past its local prefix: TGC_ERR_INVALID_ARG.
  */
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks,
                                int rank, tgc_pivot pivot, int group_m, int grid, int cta,

@@ -72,7 +72,7 @@ def _custom(R, H, K, N, cb, seed=0, sigma=1.0):
 
 
 @pytest.mark.parametrize("mode", ["fused", "unfused"])
-@pytest.mark.parametrize("pivot", ["page", "shard", "none"])
+@pytest.mark.parametrize("pivot", ["page", "shard", "none", "ready_queue"])
 def test_tiny_all_ranks(mode, pivot):
     cfg, shards, B = _inputs("tiny")
     C_ref, a_ref = _oracle_full(shards, B)
@@ -94,11 +94,11 @@ def test_ragged_shapes_full(R, H, K, N, cb):
     cfg, shards, B = _custom(R, H, K, N, cb, seed=R * H)
     C_ref, a_ref = _oracle_full(shards, B)
     run = Run(cfg, shards, B)
-    for mode in ("fused", "unfused"):
+    for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue")):
         for rank in sorted({0, R - 1}):
             run.C.zero_()
-            run(mode=mode, rank=rank)
-            assert_within_tol(run.C, C_ref, f"{mode} rank {rank}")
+            run(mode=mode, rank=rank, pivot=pivot)
+            assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank}")
             assert np.array_equal(bits16(run.a), a_ref)
 
 
@@ -148,7 +148,7 @@ def test_repeated_calls_reuse_workspace_and_flags():
     for i in range(20):
         run.C.zero_()
         run.a.view(torch.int16).fill_(-1)
-        run(rank=i % 4, pivot=["page", "shard", "none"][i % 3])
+        run(rank=i % 4, pivot=["page", "shard", "none", "ready_queue"][i % 4])
         assert_within_tol(run.C, C_ref, f"call {i}")
         assert torch.all(run.ws == 0), "workspace must be left zeroed"
 
@@ -163,7 +163,7 @@ def test_release_order_permutations_and_delays_bit_identical():
         order = torch.randperm(cfg.nblocks, generator=g).tolist()
         delay = torch.randint(0, 20000, (cfg.nblocks,), generator=g).tolist() if i % 2 else None
         run.C.zero_()
-        run(order=order, delay_ns=delay, rank=i % 4)
+        run(order=order, delay_ns=delay, rank=i % 4, pivot="ready_queue" if i % 3 == 0 else "page")
         assert torch.equal(run.C, C_unf), f"order {i}"
 
 
@@ -174,6 +174,10 @@ def test_withheld_block_times_out_and_context_survives():
     run = Run(cfg, shards, B)
     order = [c for c in range(cfg.nblocks) if c != 13]
     rc = run(order=order, spin_timeout_ns=2_000_000, check=False)
+    assert rc == _lib.TGC_ERR_TIMEOUT
+    run.ws.zero_()
+    run.progress.zero_()
+    rc = run(order=order, spin_timeout_ns=2_000_000, check=False, pivot="ready_queue")
     assert rc == _lib.TGC_ERR_TIMEOUT
     run.ws.zero_()
     run.progress.zero_()
@@ -207,3 +211,6 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     run.C.zero_()
     run(mode="mm_only")
     assert torch.equal(run.C, C_fused), "mm_only differs"
+    run.C.zero_()
+    run(mode="fused", pivot="ready_queue", **kw)
+    assert torch.equal(run.C, C_fused), "ready-queue order differs"

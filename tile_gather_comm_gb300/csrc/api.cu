@@ -36,7 +36,7 @@ int sm_count(int device) {
     return cache[device];
 }
 
-WorkspaceLayout workspace_layout(int64_t nblocks) {
+WorkspaceLayout workspace_layout(int64_t nblocks, int64_t tile_rows) {
     WorkspaceLayout w{};
     auto up = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
     w.status_off = 0;
@@ -47,9 +47,15 @@ WorkspaceLayout workspace_layout(int64_t nblocks) {
     off += up((size_t)nblocks * 4, 128);
     w.delay_off = off;
     off += up((size_t)nblocks * 4, 128);
+    w.rowcnt_off = off;
+    off += up((size_t)tile_rows * 4, 128);
+    w.ring_off = off;
+    off += up((size_t)tile_rows * 8, 128);
     w.total = off < 256 ? 256 : off;
     return w;
 }
+
+static int64_t tile_rows_of(int64_t M) { return M > 0 ? (M + kTileM - 1) / kTileM : 0; }
 
 static int elem_size(tgc_dtype dt) {
     switch (dt) {
@@ -138,7 +144,8 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.M < 0 || a.K < 0 || a.N < 0) return TGC_ERR_INVALID_ARG;
     if (a.mode != TGC_MODE_FUSED && a.mode != TGC_MODE_UNFUSED && a.mode != TGC_MODE_MM_ONLY)
         return TGC_ERR_INVALID_ARG;
-    if (a.pivot != TGC_PIVOT_PAGE && a.pivot != TGC_PIVOT_SHARD && a.pivot != TGC_PIVOT_NONE)
+    if (a.pivot != TGC_PIVOT_PAGE && a.pivot != TGC_PIVOT_SHARD && a.pivot != TGC_PIVOT_NONE &&
+        a.pivot != TGC_PIVOT_READY_QUEUE)
         return TGC_ERR_INVALID_ARG;
     if (a.M % a.nranks != 0) return TGC_ERR_INVALID_ARG;
     const int64_t rows_per_rank = a.M / a.nranks;
@@ -169,7 +176,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
         if (out.nblocks >= (int64_t(1) << 24)) return TGC_ERR_INVALID_ARG;
         if (a.progress == nullptr || !aligned(a.progress, 4)) return TGC_ERR_INVALID_ARG;
         if (a.workspace == nullptr) return TGC_ERR_WORKSPACE;
-        if (a.workspace_bytes < workspace_layout(out.nblocks).total) return TGC_ERR_WORKSPACE;
+        if (a.workspace_bytes < workspace_layout(out.nblocks, tile_rows_of(a.M)).total) return TGC_ERR_WORKSPACE;
         if (!aligned(a.workspace, 128)) return TGC_ERR_ALIGN;
         if (a.order != nullptr) {
             if (a.n_order < 0 || a.n_order > out.nblocks) return TGC_ERR_INVALID_ARG;
@@ -199,7 +206,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     const uint64_t timeout = a.spin_timeout_ns ? a.spin_timeout_ns : 2000000000ull;
 
     int32_t *status = a.d_status;
-    WorkspaceLayout wl = workspace_layout(chk.nblocks);
+    WorkspaceLayout wl = workspace_layout(chk.nblocks, tile_rows_of(a.M));
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     if (status == nullptr && ws != nullptr) status = reinterpret_cast<int32_t *>(ws + wl.status_off);
     if (a.d_status != nullptr) {
@@ -217,7 +224,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.N = a.N;
     G.cb = a.comm_block_rows;
     G.rank = a.rank;
-    G.pivot = (int)a.pivot;
+    G.pivot = (a.pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED) ? (int)TGC_PIVOT_NONE : (int)a.pivot;
     G.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
     G.grid = a.grid;
     G.timeout_ns = timeout;
@@ -232,6 +239,8 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
         G.epoch = a.epoch;
         G.ws_counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
         G.ws_tickets = reinterpret_cast<uint32_t *>(ws + wl.tickets_off);
+        G.ws_rowcnt = reinterpret_cast<uint32_t *>(ws + wl.rowcnt_off);
+        G.ws_ring = reinterpret_cast<uint64_t *>(ws + wl.ring_off);
         G.n_order = chk.nblocks;
         if (a.order != nullptr) {
             e = cudaMemcpyAsync(ws + wl.order_off, a.order, (size_t)a.n_order * 4, cudaMemcpyHostToDevice, st);
@@ -316,7 +325,7 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
     (void)N;
     int64_t nblocks = 0;
     if (nranks > 0 && comm_block_rows > 0 && M > 0) nblocks = M / comm_block_rows;
-    return workspace_layout(nblocks).total;
+    return workspace_layout(nblocks, tile_rows_of(M)).total;
 }
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args) {
@@ -356,7 +365,7 @@ int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *
     const int64_t nblocks = M / comm_block_rows;
     const size_t a_bytes = (size_t)M * (size_t)K * 2;
     const size_t p_bytes = (size_t)nblocks * 4;
-    const size_t w_bytes = workspace_layout(nblocks).total;
+    const size_t w_bytes = workspace_layout(nblocks, tile_rows_of(M)).total;
     void *d_a = nullptr, *d_p = nullptr, *d_w = nullptr;
     int dev = 0;
     cudaMemPool_t pool = nullptr;
@@ -390,7 +399,7 @@ int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, in
     if (M <= 0 || N <= 0 || nranks <= 0 || M % nranks != 0 || rank < 0 || rank >= nranks || grid <= 0 ||
         cta < 0 || cta >= grid || group_m < 0 || comm_block_rows <= 0)
         return TGC_ERR_INVALID_ARG;
-    if (pivot != TGC_PIVOT_PAGE && pivot != TGC_PIVOT_SHARD && pivot != TGC_PIVOT_NONE) return TGC_ERR_INVALID_ARG;
+    if (pivot != TGC_PIVOT_PAGE && pivot != TGC_PIVOT_SHARD && pivot != TGC_PIVOT_NONE) return TGC_ERR_INVALID_ARG;  // READY_QUEUE is dynamic
     TileSchedule s{};
     s.num_pid_m = (int)((M + kTileM - 1) / kTileM);
     s.num_pid_n = (int)((N + kBN - 1) / kBN);

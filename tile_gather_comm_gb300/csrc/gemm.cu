@@ -119,8 +119,15 @@ struct GemmParams {
     const int32_t *order;      // device copy in the workspace, or null
     const uint32_t *delay_ns;  // device copy in the workspace, or null
     uint32_t *counters;
-    uint32_t *tickets;
+    uint32_t *tickets;   // [0] piece ticket, [1] finished producers, [2] ready-ring tail, [3] finished CTAs
     uint64_t *trace;  // optional: kTraceWords per CTA
+    // ready-queue order (FUSED only)
+    int rq;               // nonzero: READY_QUEUE tile order
+    int rq_local_row0;    // first tile row lying entirely inside the caller's shard
+    int rq_local_rows;    // number of such tile rows (they come first)
+    int tile_m;           // rows per tile (cluster)
+    uint32_t *rowcnt;     // released blocks per tile row
+    uint64_t *ring;       // tile rows in the order they became complete
 };
 
 // Trace word indices (mirrors TGC_TRACE_* in tgc.h).
@@ -158,6 +165,74 @@ __device__ int wait_blocks(const GemmParams &p, int b0, int b1, int lane) {
     return waited;
 }
 
+// ---------------------------------------------------------------- tile order
+
+// Position `pos` of the persistent walk -> tile.  Static orders map it with
+// the swizzle + pivot of TileSchedule.  READY_QUEUE maps the first
+// rq_local_rows * num_pid_n positions to the rows inside the caller's shard
+// (swizzled), and position q past that prefix to column-major chunks of
+// group_m ready-ring rows: ring slot `ring_idx` then names the tile row, known
+// only once the producer has appended it.
+struct TilePos {
+    int pid_m, pid_n;
+    int ring_idx;  // >= 0: pid_m comes from ring[ring_idx]
+};
+
+__device__ __forceinline__ TilePos tile_at(const GemmParams &p, int pos) {
+    TilePos r;
+    r.ring_idx = -1;
+    if (!p.rq) {
+        p.sched.tile(pos, r.pid_m, r.pid_n);
+        return r;
+    }
+    const int npn = p.sched.num_pid_n;
+    const int n_local = p.rq_local_rows * npn;
+    if (pos < n_local) {
+        TileSchedule s = p.sched;
+        s.num_pid_m = p.rq_local_rows;
+        s.pivot_off = 0;
+        s.tile(pos, r.pid_m, r.pid_n);
+        r.pid_m += p.rq_local_row0;
+        return r;
+    }
+    const int q = pos - n_local;
+    const int G = p.sched.group_m;
+    const int nrem = p.sched.num_pid_m - p.rq_local_rows;
+    const int chunk = q / (G * npn);
+    const int rows = (nrem - chunk * G) < G ? (nrem - chunk * G) : G;
+    const int rr = q - chunk * G * npn;
+    r.ring_idx = chunk * G + rr % rows;
+    r.pid_n = rr / rows;
+    r.pid_m = -1;
+    return r;
+}
+
+// Warp-collective: tile row stored in ring[idx] for this call's epoch, or -1
+// if the wait was abandoned (timeout or abort).  Sets *waited if it spun.
+__device__ int ring_row(const GemmParams &p, int idx, int lane, bool *waited) {
+    int row = -1;
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint64_t it = 0; it < (1ull << 36); ++it) {
+            const uint64_t e = ld_acquire_gpu_u64(p.ring + idx);
+            if ((uint32_t)(e >> 32) == p.epoch && (uint32_t)e != 0u) {
+                row = (int)(uint32_t)e - 1;
+                break;
+            }
+            *waited = true;
+            if ((it & 7) == 7) {
+                if (ld_status(p.status) != 0) break;
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    raise_status(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+            __nanosleep(32);
+        }
+    }
+    return __shfl_sync(0xffffffffu, row, 0);
+}
+
 // ---------------------------------------------------------------- roles
 
 // Cluster-tile index space: cluster c of nclusters persistent clusters (a
@@ -178,8 +253,18 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     // completion of every stage is counted on the even CTA's full barrier
     const uint32_t full0 = CG == 2 ? mapa_shared(smem_addr(full), 0) : smem_addr(full);
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>()) {
-        int pid_m, pid_n;
-        p.sched.tile(t, pid_m, pid_n);
+        TilePos tp = tile_at(p, t);
+        if (tp.ring_idx >= 0) {
+            bool spun = false;
+            const uint64_t w0 = p.trace != nullptr ? globaltimer_ns() : 0;
+            tp.pid_m = ring_row(p, tp.ring_idx, lane, &spun);
+            if (tp.pid_m < 0) { ok = false; break; }
+            if (p.trace != nullptr && spun) {
+                wait_ns += globaltimer_ns() - w0;
+                ++waited_tiles;
+            }
+        }
+        const int pid_m = tp.pid_m, pid_n = tp.pid_n;
         const int m0 = pid_m * C::kTileM + (int)crank * C::kRowsCta;  // this CTA's 128 rows
         const int nb = pid_n * kBN + (int)crank * C::kHalfN;          // this CTA's B rows
         const CUtensorMap *mapA = tmA;
@@ -291,13 +376,18 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
     const uint32_t tempty0 = CG == 2 ? mapa_shared(smem_addr(tempty), 0) : smem_addr(tempty);
     uint32_t tc = 0;
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>(), ++tc) {
-        int pid_m, pid_n;
-        p.sched.tile(t, pid_m, pid_n);
+        TilePos tp = tile_at(p, t);
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&tfull[acc], aph, p.status, p.mbar_timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform: tcgen05.ld is .sync.aligned
         if (!ok) break;
+        if (tp.ring_idx >= 0) {  // already published: the loads of this tile waited for it
+            bool spun = false;
+            tp.pid_m = ring_row(p, tp.ring_idx, lane, &spun);
+            if (tp.pid_m < 0) break;
+        }
+        const int pid_m = tp.pid_m, pid_n = tp.pid_n;
         tc_fence_after();
         const int m = pid_m * C::kTileM + (int)crank * C::kRowsCta + row;
         const int n0 = pid_n * kBN;
@@ -368,6 +458,25 @@ __device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticke
         st_relaxed_gpu(p.counters + pc.block, 0u);  // every piece of this block is counted
         if (p.delay_ns != nullptr) spin_for_ns(p.delay_ns[pc.block]);
         st_release_gpu(p.progress + pc.block, p.epoch);
+        if (p.rq) {
+            // tile rows this block completes go to the ready ring (rows inside
+            // the caller's shard are never queued: they come first anyway)
+            const int64_t b_row0 = (int64_t)pc.block * p.cb;
+            const int r0 = (int)(b_row0 / p.tile_m);
+            const int r1 = (int)((b_row0 + p.cb - 1) / p.tile_m);
+            for (int r = r0; r <= r1 && r < p.sched.num_pid_m; ++r) {
+                if (r >= p.rq_local_row0 && r < p.rq_local_row0 + p.rq_local_rows) continue;
+                const int64_t lo = (int64_t)r * p.tile_m;
+                const int64_t hi = (lo + p.tile_m < p.M ? lo + p.tile_m : p.M) - 1;
+                const uint32_t need = (uint32_t)(hi / p.cb - lo / p.cb + 1);  // blocks covering row r
+                const uint32_t o = atom_add_acq_rel_gpu(p.rowcnt + r, 1u);
+                if (o + 1 == need) {
+                    st_relaxed_gpu(p.rowcnt + r, 0u);
+                    const uint32_t slot = atom_add_relaxed_gpu(p.tickets + 2, 1u);
+                    st_release_gpu_u64(p.ring + slot, ((uint64_t)p.epoch << 32) | (uint64_t)(r + 1));
+                }
+            }
+        }
     }
 }
 
@@ -475,6 +584,7 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
         if (done + 1 == gridDim.x) {
             st_relaxed_gpu(p.tickets, 0u);
             st_relaxed_gpu(p.tickets + 1, 0u);
+            st_relaxed_gpu(p.tickets + 2, 0u);
         }
     } else {
         for (uint32_t i = head; i < tail; ++i) mbar_drain_wait(&slotbar[i % kSlots], (i / kSlots) & 1u, kDrainTimeoutNs);
@@ -553,6 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (CG == 1) tmem_dealloc(tmem_base, kTmemCols);
         else tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+    if (FUSED && p.rq && threadIdx.x == 0 && ld_status(p.status) == 0) {
+        // every warp of this CTA is past its last ring read; the last CTA to
+        // get here clears the ring so that the workspace is zero again
+        const uint32_t done = atom_add_acq_rel_gpu(p.tickets + 3, 1u);
+        if (done + 1 == gridDim.x) {
+            for (int r = 0; r < p.sched.num_pid_m; ++r) p.ring[r] = 0ull;
+            st_relaxed_gpu(p.tickets + 3, 0u);
+        }
     }
 }
 
@@ -699,6 +818,22 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.delay_ns = L.delay_ns;
         p.counters = L.ws_counters;
         p.tickets = L.ws_tickets;
+        p.tile_m = C::kTileM;
+        p.rowcnt = L.ws_rowcnt;
+        p.ring = L.ws_ring;
+        if (L.pivot == TGC_PIVOT_READY_QUEUE) {
+            p.rq = 1;
+            p.sched.pivot_off = 0;
+            // tile rows lying entirely inside [local_row0, local_row1)
+            const int64_t r0 = (p.local_row0 + C::kTileM - 1) / C::kTileM;
+            int64_t r1 = p.local_row1 / C::kTileM;  // exclusive
+            if (p.local_row1 == p.M) r1 = p.sched.num_pid_m;  // a partial last row inside the shard
+            p.rq_local_row0 = (int)r0;
+            p.rq_local_rows = (int)(r1 > r0 ? r1 - r0 : 0);
+            if (p.rq_local_rows == 0) p.rq_local_row0 = 0;
+            // releases follow the ring's natural consumer: rows after the local prefix, in order
+            p.first_block = (int)((r1 < p.sched.num_pid_m ? r1 : 0) * C::kTileM / L.cb);
+        }
     } else {
         tmL = tmA;
     }

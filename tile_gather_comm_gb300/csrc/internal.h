@@ -55,7 +55,9 @@ struct GemmLaunch {
     const uint32_t *delay_ns;
     uint64_t timeout_ns;
     uint32_t *ws_counters;  // nblocks
-    uint32_t *ws_tickets;   // [0] piece ticket, [1] finished producers
+    uint32_t *ws_tickets;   // [0] piece ticket, [1] finished producers, [2] ready-ring tail, [3] finished CTAs
+    uint32_t *ws_rowcnt;    // tile rows (READY_QUEUE)
+    uint64_t *ws_ring;      // tile rows (READY_QUEUE)
     int32_t *status;
     uint64_t *trace;        // optional, kTraceWords per CTA
 };
@@ -72,12 +74,14 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out);
 // Workspace layout of tgc_ag_matmul_ex.
 struct WorkspaceLayout {
     size_t status_off;    // int32 status word
-    size_t tickets_off;   // 2 x uint32
+    size_t tickets_off;   // uint32 x 4: piece ticket, finished producers, ready-ring tail, finished CTAs
     size_t counters_off;  // nblocks x uint32 piece counters
     size_t order_off;     // nblocks x int32: device copy of the release order
     size_t delay_off;     // nblocks x uint32: device copy of the release delays
+    size_t rowcnt_off;    // tile_rows x uint32: released blocks per tile row
+    size_t ring_off;      // tile_rows x uint64: ready ring, (epoch << 32) | (row + 1)
     size_t total;
 };
-WorkspaceLayout workspace_layout(int64_t nblocks);
+WorkspaceLayout workspace_layout(int64_t nblocks, int64_t tile_rows);
 
 }  // namespace tgc

@@ -62,9 +62,9 @@ struct ScratchLayout {
     size_t total;
 };
 
-ScratchLayout scratch_layout(int64_t nblocks) {
+ScratchLayout scratch_layout(int64_t nblocks, int64_t M) {
     ScratchLayout l{};
-    l.ws_bytes = workspace_layout(nblocks).total;
+    l.ws_bytes = workspace_layout(nblocks, M > 0 ? (M + kTileM - 1) / kTileM : 0).total;
     l.progress_off = (l.ws_bytes + 255) / 256 * 256;
     l.total = l.progress_off + (size_t)nblocks * 4;
     return l;
@@ -108,11 +108,11 @@ extern "C" int tgc_ag_matmul_noalloc(const void *const *a_shards, int nranks, co
         if (rc == 1) return TGC_OK;  // empty problem
         if (rc < 0 && rc != TGC_ERR_WORKSPACE) return rc;
         if (rc == TGC_ERR_WORKSPACE || chk.nblocks > kNoAllocMaxBlocks ||
-            scratch_layout(chk.nblocks).total > kNoAllocScratchBytes)
+            scratch_layout(chk.nblocks, M).total > kNoAllocScratchBytes)
             return TGC_ERR_TOO_LARGE;
     }
     const int64_t nblocks = M / comm_block_rows;
-    const ScratchLayout l = scratch_layout(nblocks);
+    const ScratchLayout l = scratch_layout(nblocks, M);
 
     uint8_t *base = nullptr;
     int rc = scratch_address(&base);

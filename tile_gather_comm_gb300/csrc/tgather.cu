@@ -8,9 +8,11 @@
 // GPU design.  With dense tensors, the H*W elements of rank r in slab
 // (d0,d1,d2) are ONE contiguous run in the source and ONE contiguous run in
 // the destination, so the whole gather is nranks*D0*D1*D2 contiguous copies.
-// Each run is cut into segments (one per progress chunk, or the whole run),
-// each segment into tiles of TILE_VECS vectors; a persistent grid walks the
-// (segment, tile) items.  Copies go through registers with VW-byte vectors
+// Without progress release (tgather_flat_kernel) each CTA of one full wave
+// copies an equal byte share of the concatenated runs.  With progress release
+// (tgather_kernel) each run is cut into segments, one per progress chunk, each
+// segment into tiles of kTGThreads*kTGUnroll vectors, and a persistent grid
+// walks the (segment, tile) items.  Copies go through registers with VW-byte vectors
 // (16 bytes whenever the source and destination agree modulo 16), coalesced:
 // consecutive threads touch consecutive vectors.  The unaligned head and the
 // ragged tail of a segment (fewer than VW bytes each) are copied element by
@@ -30,8 +32,22 @@
 
 namespace tgc {
 
-constexpr int kTGThreads = 256;
-constexpr int kTGUnroll = 4;
+// Compile-time tuning (defaults chosen by measurement on GB300).
+#ifndef TGC_TG_THREADS
+#define TGC_TG_THREADS 256   // threads per CTA
+#endif
+#ifndef TGC_TG_UNROLL
+#define TGC_TG_UNROLL 8      // vectors in flight per thread
+#endif
+#ifndef TGC_TG_FLAT
+#define TGC_TG_FLAT 1        // equal byte shares per CTA (1) or 16 KiB items (0)
+#endif
+#ifndef TGC_TG_PDL
+#define TGC_TG_PDL 1         // programmatic dependent launch for the flat kernel
+#endif
+
+constexpr int kTGThreads = TGC_TG_THREADS;
+constexpr int kTGUnroll = TGC_TG_UNROLL;
 
 struct TGParams {
     const uint8_t *srcs[TGC_MAX_RANKS];
@@ -142,6 +158,61 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
     }
 }
 
+// Flat variant (no progress release): the work space is the concatenation of
+// all (slab, rank) runs, and CTA c copies the c-th of gridDim.x equal,
+// 16-byte-aligned shares of it -- every CTA moves the same number of bytes,
+// so a grid of whole waves finishes together.  A share may span several runs;
+// each (run, share) intersection is copied with VW-byte vectors between
+// element-wise heads and tails.  The kernel is launched with programmatic
+// stream serialization: it lets the next launch in the stream be scheduled as
+// soon as every CTA has started, and waits for the previous grid's completion
+// (griddepcontrol.wait) before touching memory.
+template <int VW>
+__global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams p, int64_t share) {
+    using V = typename VecT<VW>::T;
+#if TGC_TG_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+    const int tid = threadIdx.x;
+    const int64_t total = p.nslab * p.nranks * p.run_bytes;
+    int64_t lo = (int64_t)blockIdx.x * share;
+    const int64_t hi = lo + share < total ? lo + share : total;
+    while (lo < hi) {
+        const int64_t run = lo / p.run_bytes;         // run = slab * nranks + r
+        const int64_t off = lo - run * p.run_bytes;   // offset inside the run
+        const int64_t end_in_run = (hi - run * p.run_bytes) < p.run_bytes ? (hi - run * p.run_bytes) : p.run_bytes;
+        const int64_t len = end_in_run - off;
+        const int64_t slab = run / p.nranks;
+        const int r = (int)(run - slab * p.nranks);
+        const uint8_t *src = p.srcs[r] + slab * p.run_bytes + off;
+        uint8_t *dst = p.dst + slab * p.dst_slab_bytes + (int64_t)r * p.run_bytes + off;
+
+        int64_t head = (int64_t)((VW - (reinterpret_cast<uintptr_t>(src) % VW)) % VW);
+        if (head > len) head = len;
+        const int64_t nvec = (len - head) / VW;
+        const int64_t body_end = head + nvec * VW;
+        const V *vs = reinterpret_cast<const V *>(src + head);
+        V *vd = reinterpret_cast<V *>(dst + head);
+        for (int64_t base = 0; base < nvec; base += (int64_t)kTGThreads * kTGUnroll) {
+            V reg[kTGUnroll];
+#pragma unroll
+            for (int k = 0; k < kTGUnroll; ++k) {
+                const int64_t idx = base + tid + (int64_t)k * kTGThreads;
+                if (idx < nvec) reg[k] = ld_stream(vs + idx);
+            }
+#pragma unroll
+            for (int k = 0; k < kTGUnroll; ++k) {
+                const int64_t idx = base + tid + (int64_t)k * kTGThreads;
+                if (idx < nvec) vd[idx] = reg[k];
+            }
+        }
+        if (head > 0) copy_elems(dst, src, head, p.es, tid, kTGThreads);
+        if (len > body_end) copy_elems(dst + body_end, src + body_end, len - body_end, p.es, tid, kTGThreads);
+        lo += len;
+    }
+}
+
 static int pick_vw(const TGatherLaunch &L) {
     // Largest power of two <= 16 dividing every (src - dst) address difference;
     // then source and destination share their alignment modulo VW everywhere.
@@ -185,6 +256,36 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     const int64_t slots = (int64_t)sm_count(dev) * (2048 / kTGThreads);
+
+    if (TGC_TG_FLAT && L.progress == nullptr) {
+        // equal 16-byte-aligned shares over one full wave (or fewer CTAs for small copies)
+        const int64_t total = L.nslab * L.nranks * L.run_bytes;
+        const int64_t min_share = (int64_t)kTGThreads * kTGUnroll * 16;  // 16 KiB
+        int64_t grid = (total + min_share - 1) / min_share;
+        if (grid > slots) grid = slots;
+        if (grid < 1) grid = 1;
+        int64_t share = (total + grid - 1) / grid;
+        share = (share + 15) / 16 * 16;
+        grid = (total + share - 1) / share;
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(kTGThreads, 1, 1);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = TGC_TG_PDL ? 1 : 0;
+        switch (vw) {
+            case 16: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<16>, p, share); break;
+            case 8: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<8>, p, share); break;
+            case 4: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<4>, p, share); break;
+            case 2: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<2>, p, share); break;
+            default: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<1>, p, share); break;
+        }
+        if (e == cudaSuccess) e = cudaGetLastError();
+        return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+    }
     const int64_t waves = (p.total_items + slots - 1) / slots;
     const int64_t grid = (p.total_items + waves - 1) / waves;
 
