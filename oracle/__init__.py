@@ -41,12 +41,7 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
-def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
+def _bind(lib):
     i64, vp = ctypes.c_int64, ctypes.c_void_p
     lib.oracle_tgather.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int,
                                    i64, i64, i64, i64, i64, i64, i64]
@@ -69,8 +64,15 @@ def _load():
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     lib.oracle_set_num_threads.restype = None
-    _lib = lib
     return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -82,112 +84,163 @@ def _ptr_array(arrs):
     return (ctypes.c_void_p * len(arrs))(*[_ptr(a) for a in arrs])
 
 
+class Oracle:
+    """The oracle's functions bound to one compiled copy of oracle.c (the
+    default build, or a deliberately broken copy that a test compiles to show
+    that the pins catch a planted mistake)."""
+
+    def __init__(self, lib):
+        self._L = lib
+
+    def num_threads(self) -> int:
+        return self._L.oracle_num_threads()
+
+    def set_num_threads(self, n: int) -> None:
+        self._L.oracle_set_num_threads(int(n))
+
+    def tgather(self, srcs, dst_rows3: int | None = None, dst: np.ndarray | None = None) -> np.ndarray:
+        """[TG] §二: dst[d0,d1,d2, r*H+i, j] = srcs[r][d0,d1,d2,i,j].
+
+        ``srcs`` are N numpy arrays of identical 5-D shape (D0,D1,D2,H,W) and dtype.
+        ``dst_rows3`` (>= N*H) gives dst's DIM_3 ([TG] §7.2); rows past N*H are left
+        as they are in ``dst`` (zeros when ``dst`` is not given).
+        """
+        lib = self._L
+        srcs = [np.ascontiguousarray(s) for s in srcs]
+        n = len(srcs)
+        if n == 0:
+            raise ValueError("nranks must be > 0")
+        shape, dt = srcs[0].shape, srcs[0].dtype
+        if len(shape) != 5 or any(s.shape != shape or s.dtype != dt for s in srcs):
+            raise ValueError("all sources must share one 5-D shape and dtype")
+        D0, D1, D2, H, W = shape
+        rows = n * H if dst_rows3 is None else int(dst_rows3)
+        if dst is None:
+            dst = np.zeros((D0, D1, D2, rows, W), dtype=dt)
+        assert dst.shape == (D0, D1, D2, rows, W) and dst.dtype == dt
+        rc = lib.oracle_tgather(_ptr(dst), _ptr_array(srcs), n, D0, D1, D2, H, W,
+                                dt.itemsize, rows)
+        if rc != 0:
+            raise ValueError(f"oracle_tgather rejected the arguments (rc={rc})")
+        return dst
+
+    def bf16_to_f32(self, bits: np.ndarray) -> np.ndarray:
+        """Widen bf16 bit patterns (uint16) to float32: the bits go to the upper half."""
+        bits = np.asarray(bits, dtype=np.uint16)
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+
+    def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
+        """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.uint16)
+        self._L.oracle_f32_to_bf16_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def f32_to_bf16_scalar(self, x: float) -> int:
+        return int(self._L.oracle_f32_to_bf16_rne(ctypes.c_float(x)))
+
+    def ag_matmul(self, a_shards, B: np.ndarray):
+        """[AGM]: a = TGATHER(a_shards) (M,K); C = bf16(a @ B^T) with fp32 accumulation.
+
+        ``a_shards``: R uint16 arrays (M/R, K); ``B``: uint16 (N, K).  Returns (C, a).
+        """
+        lib = self._L
+        shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
+        R = len(shards)
+        Hs, K = shards[0].shape
+        M = R * Hs
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        N = B.shape[0]
+        assert B.shape == (N, K)
+        C = np.zeros((M, N), dtype=np.uint16)
+        a = np.zeros((M, K), dtype=np.uint16)
+        rc = lib.oracle_ag_matmul(_ptr_array(shards), R, _ptr(B), _ptr(C), _ptr(a), M, K, N)
+        if rc != 0:
+            raise ValueError(f"oracle_ag_matmul rejected the arguments (rc={rc})")
+        return C, a
+
+    def ag_matmul_rows(self, a_shards, B: np.ndarray, rows) -> np.ndarray:
+        """The rows ``rows`` of C only (each computed exactly as in ag_matmul)."""
+        lib = self._L
+        shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
+        R = len(shards)
+        Hs, K = shards[0].shape
+        M = R * Hs
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        N = B.shape[0]
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.zeros((rows.size, N), dtype=np.uint16)
+        rc = lib.oracle_ag_matmul_rows(_ptr_array(shards), R, _ptr(B), M, K, N,
+                                       _ptr(rows), rows.size, _ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle_ag_matmul_rows rejected the arguments (rc={rc})")
+        return out
+
+    def ag_matmul_chunked(self, a_shards, B: np.ndarray, cb: int, order):
+        """Block-by-block producer/consumer walk in release order ``order``; returns (C, a)."""
+        lib = self._L
+        shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
+        R = len(shards)
+        Hs, K = shards[0].shape
+        M = R * Hs
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        N = B.shape[0]
+        order = np.ascontiguousarray(order, dtype=np.int64)
+        C = np.zeros((M, N), dtype=np.uint16)
+        a = np.zeros((M, K), dtype=np.uint16)
+        rc = lib.oracle_ag_matmul_chunked(_ptr_array(shards), R, _ptr(B), _ptr(C), _ptr(a),
+                                          M, K, N, int(cb), _ptr(order), order.size)
+        if rc != 0:
+            raise ValueError(f"oracle_ag_matmul_chunked rejected the arguments (rc={rc})")
+        return C, a
+
+
+def load_from(path: str) -> Oracle:
+    """An Oracle over another compiled copy of oracle.c (used by the mutation tests)."""
+    return Oracle(_bind(ctypes.CDLL(path)))
+
+
+_default = None
+
+
+def _oracle() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(_load())
+    return _default
+
+
 def num_threads() -> int:
-    return _load().oracle_num_threads()
+    return _oracle().num_threads()
 
 
 def set_num_threads(n: int) -> None:
-    _load().oracle_set_num_threads(int(n))
+    _oracle().set_num_threads(n)
 
 
-def tgather(srcs, dst_rows3: int | None = None, dst: np.ndarray | None = None) -> np.ndarray:
-    """[TG] §二: dst[d0,d1,d2, r*H+i, j] = srcs[r][d0,d1,d2,i,j].
-
-    ``srcs`` are N numpy arrays of identical 5-D shape (D0,D1,D2,H,W) and dtype.
-    ``dst_rows3`` (>= N*H) gives dst's DIM_3 ([TG] §7.2); rows past N*H are left
-    as they are in ``dst`` (zeros when ``dst`` is not given).
-    """
-    lib = _load()
-    srcs = [np.ascontiguousarray(s) for s in srcs]
-    n = len(srcs)
-    if n == 0:
-        raise ValueError("nranks must be > 0")
-    shape, dt = srcs[0].shape, srcs[0].dtype
-    if len(shape) != 5 or any(s.shape != shape or s.dtype != dt for s in srcs):
-        raise ValueError("all sources must share one 5-D shape and dtype")
-    D0, D1, D2, H, W = shape
-    rows = n * H if dst_rows3 is None else int(dst_rows3)
-    if dst is None:
-        dst = np.zeros((D0, D1, D2, rows, W), dtype=dt)
-    assert dst.shape == (D0, D1, D2, rows, W) and dst.dtype == dt
-    rc = lib.oracle_tgather(_ptr(dst), _ptr_array(srcs), n, D0, D1, D2, H, W,
-                            dt.itemsize, rows)
-    if rc != 0:
-        raise ValueError(f"oracle_tgather rejected the arguments (rc={rc})")
-    return dst
+def tgather(srcs, dst_rows3=None, dst=None):
+    return _oracle().tgather(srcs, dst_rows3=dst_rows3, dst=dst)
 
 
-def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
-    """Widen bf16 bit patterns (uint16) to float32: the bits go to the upper half."""
-    bits = np.asarray(bits, dtype=np.uint16)
-    return (bits.astype(np.uint32) << 16).view(np.float32)
+def bf16_to_f32(bits):
+    return _oracle().bf16_to_f32(bits)
 
 
-def f32_to_bf16(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty(x.shape, dtype=np.uint16)
-    _load().oracle_f32_to_bf16_array(_ptr(x), _ptr(y), x.size)
-    return y
+def f32_to_bf16(x):
+    return _oracle().f32_to_bf16(x)
 
 
-def f32_to_bf16_scalar(x: float) -> int:
-    return int(_load().oracle_f32_to_bf16_rne(ctypes.c_float(x)))
+def f32_to_bf16_scalar(x):
+    return _oracle().f32_to_bf16_scalar(x)
 
 
-def ag_matmul(a_shards, B: np.ndarray):
-    """[AGM]: a = TGATHER(a_shards) (M,K); C = bf16(a @ B^T) with fp32 accumulation.
-
-    ``a_shards``: R uint16 arrays (M/R, K); ``B``: uint16 (N, K).  Returns (C, a).
-    """
-    lib = _load()
-    shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
-    R = len(shards)
-    Hs, K = shards[0].shape
-    M = R * Hs
-    B = np.ascontiguousarray(B, dtype=np.uint16)
-    N = B.shape[0]
-    assert B.shape == (N, K)
-    C = np.zeros((M, N), dtype=np.uint16)
-    a = np.zeros((M, K), dtype=np.uint16)
-    rc = lib.oracle_ag_matmul(_ptr_array(shards), R, _ptr(B), _ptr(C), _ptr(a), M, K, N)
-    if rc != 0:
-        raise ValueError(f"oracle_ag_matmul rejected the arguments (rc={rc})")
-    return C, a
+def ag_matmul(a_shards, B):
+    return _oracle().ag_matmul(a_shards, B)
 
 
-def ag_matmul_rows(a_shards, B: np.ndarray, rows) -> np.ndarray:
-    """The rows ``rows`` of C only (each computed exactly as in ag_matmul)."""
-    lib = _load()
-    shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
-    R = len(shards)
-    Hs, K = shards[0].shape
-    M = R * Hs
-    B = np.ascontiguousarray(B, dtype=np.uint16)
-    N = B.shape[0]
-    rows = np.ascontiguousarray(rows, dtype=np.int64)
-    out = np.zeros((rows.size, N), dtype=np.uint16)
-    rc = lib.oracle_ag_matmul_rows(_ptr_array(shards), R, _ptr(B), M, K, N,
-                                   _ptr(rows), rows.size, _ptr(out))
-    if rc != 0:
-        raise ValueError(f"oracle_ag_matmul_rows rejected the arguments (rc={rc})")
-    return out
+def ag_matmul_rows(a_shards, B, rows):
+    return _oracle().ag_matmul_rows(a_shards, B, rows)
 
 
-def ag_matmul_chunked(a_shards, B: np.ndarray, cb: int, order):
-    """Block-by-block producer/consumer walk in release order ``order``; returns (C, a)."""
-    lib = _load()
-    shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
-    R = len(shards)
-    Hs, K = shards[0].shape
-    M = R * Hs
-    B = np.ascontiguousarray(B, dtype=np.uint16)
-    N = B.shape[0]
-    order = np.ascontiguousarray(order, dtype=np.int64)
-    C = np.zeros((M, N), dtype=np.uint16)
-    a = np.zeros((M, K), dtype=np.uint16)
-    rc = lib.oracle_ag_matmul_chunked(_ptr_array(shards), R, _ptr(B), _ptr(C), _ptr(a),
-                                      M, K, N, int(cb), _ptr(order), order.size)
-    if rc != 0:
-        raise ValueError(f"oracle_ag_matmul_chunked rejected the arguments (rc={rc})")
-    return C, a
+def ag_matmul_chunked(a_shards, B, cb, order):
+    return _oracle().ag_matmul_chunked(a_shards, B, cb, order)
