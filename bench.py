@@ -190,6 +190,30 @@ class ClockSampler:
                 "reasons": reasons}
 
 
+def time_interleaved(variants: dict, steps: int, dist: Dist, stream, rounds: int = 6):
+    """Median ms per call of each variant, timed in alternating rounds of ~steps/rounds calls."""
+    import torch
+    per = max(2, steps // rounds)
+    names = list(variants)
+    for n in names:
+        for _ in range(2):
+            variants[n]()
+    torch.cuda.synchronize()
+    times = {n: [] for n in names}
+    for r in range(rounds):
+        for n in (names if r % 2 == 0 else names[::-1]):
+            dist.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(per):
+                variants[n]()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[n].append(e0.elapsed_time(e1) / per)
+    return {n: statistics.median(v) for n, v in times.items()}
+
+
 def time_device(fn, steps: int, warmup: int, dist: Dist, stream):
     """Barrier + sync, then CUDA events on `stream` around exactly `steps` calls."""
     import torch
@@ -253,11 +277,12 @@ def run_ours(args, dist: Dist):
     epoch = [0]
     launches = [0]
 
-    def call(mode="fused", delays=True):
+    def call(mode="fused", delays=True, pivot="page"):
         epoch[0] += 1
         tgc.tgc_ag_matmul_ex(shards, B, C, a, cfg.cb, mode=mode, progress=progress, epoch=epoch[0],
                              workspace=ws, order=order if mode == "fused" else None,
-                             delay_ns=delay if (mode == "fused" and delays) else None, stream=stream)
+                             delay_ns=delay if (mode == "fused" and delays) else None, stream=stream,
+                             pivot=pivot)
         launches[0] += 2 if mode == "unfused" else 1
 
     sampler = ClockSampler(dist.local_rank, args.clock_ms)
@@ -290,30 +315,74 @@ def run_ours(args, dist: Dist):
                        "kernel": "ag_gemm_kernel<fused>"}
 
     if not args.quick:
-        ms_unf = time_device(lambda: call("unfused"), args.steps, args.warmup, dist, stream)
-        ms_mm = time_device(lambda: call("mm_only"), args.steps, args.warmup, dist, stream)
-        res["unfused"] = {"value": round(aggregate(ms_unf, flops, dist)[0], 2), "unit": "TFLOP/s",
-                          "ms_per_step": round(dist.max(ms_unf), 4), "kernels_per_step": 2}
-        res["mm_only"] = {"value": round(aggregate(ms_mm, flops, dist)[0], 2), "unit": "TFLOP/s",
-                          "ms_per_step": round(dist.max(ms_mm), 4),
-                          "frac_of_peak": round(flops / (ms_mm * 1e-3) * 1e-12 / peaks["bf16_tflops"], 4)}
-        res["fused_over_unfused"] = round(ms_unf / ms_fused, 4)
+        # The comparison lines are timed interleaved (rounds of every variant, median per
+        # variant), so that slow drifts of the power-capped clock do not bias their ratios.
+        variants = {"fused": lambda: call("fused"), "unfused": lambda: call("unfused"),
+                    "mm_only": lambda: call("mm_only"),
+                    "ready_queue": lambda: call("fused", pivot="ready_queue")}
         if cfg.skewed:
-            ms_nd = time_device(lambda: call("fused", delays=False), args.steps, args.warmup, dist, stream)
-            res["no_delay"] = {"value": round(aggregate(ms_nd, flops, dist)[0], 2), "unit": "TFLOP/s",
-                               "ms_per_step": round(dist.max(ms_nd), 4)}
+            variants["no_delay"] = lambda: call("fused", delays=False)
+        med = time_interleaved(variants, args.steps, dist, stream)
+        for k, v in med.items():
+            res[k if k != "fused" else "fused_interleaved"] = {
+                "value": round(aggregate(v, flops, dist)[0], 2), "unit": "TFLOP/s",
+                "ms_per_step": round(dist.max(v), 4)}
+        res["unfused"]["kernels_per_step"] = 2
+        res["mm_only"]["frac_of_peak"] = round(flops / (med["mm_only"] * 1e-3) * 1e-12 / peaks["bf16_tflops"], 4)
+        res["ready_queue"]["note"] = "same workload, READY_QUEUE tile order"
+        res["fused_over_unfused"] = round(med["unfused"] / med["fused"], 4)
+        res["comparison_timing"] = "interleaved rounds (6), median per variant"
         res["tgather"] = bench_tgather(TG_CONFIGS["bw_f16"], dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_ragged_i32"] = bench_tgather(TG_CONFIGS["ragged_i32"], dev, stream, dist, peaks,
                                                   peaks_kind, args)
     res["clocks"] = sampler.stop()
 
     if not args.quick:
+        res["other_workloads"] = bench_other_workloads(dev, stream, dist, args, peaks)
         res["e2e"] = bench_e2e(cfg, shards_h, B_h, a, progress, ws, order, delay, dev, stream, dist, args)
         if dist.rank == 0 and dist.world == 1:
             res["cpu_baseline"] = cpu_baseline(cfg, shards_h, B_h)
     del shards, B, C, a
     torch.cuda.empty_cache()
     return res
+
+
+def bench_other_workloads(dev, stream, dist, args, peaks):
+    """The square and MLP-up AllGather-MatMul workloads: fused (page pivot), fused (ready
+    queue), unfused and mm_only, TFLOP/s, timed interleaved.  Their inputs (up to 0.5 GB)
+    also exceed L2."""
+    import torch
+
+    import tile_gather_comm_gb300 as tgc
+    from tile_gather_comm_gb300.workloads import AG_CONFIGS, make_ag_inputs
+
+    out = {}
+    for name in ("square", "mlp_up"):
+        cfg = AG_CONFIGS[name]
+        sh, Bh = make_ag_inputs(cfg, seed=0)
+        shards = [x.to(dev) for x in sh]
+        B = Bh.to(dev)
+        C = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)
+        a = torch.empty(cfg.M, cfg.K, dtype=torch.bfloat16, device=dev)
+        progress = torch.zeros(cfg.nblocks, dtype=torch.int32, device=dev)
+        ws = torch.zeros(tgc.tgc_ag_matmul_workspace_bytes(cfg.R, cfg.M, cfg.K, cfg.N, cfg.cb),
+                         dtype=torch.uint8, device=dev)
+        ep = [0]
+
+        def call(mode, pivot="page"):
+            ep[0] += 1
+            tgc.tgc_ag_matmul_ex(shards, B, C, a, cfg.cb, mode=mode, pivot=pivot, progress=progress,
+                                 epoch=ep[0], workspace=ws, stream=stream)
+        med = time_interleaved({"fused": lambda: call("fused"),
+                                "fused_ready_queue": lambda: call("fused", "ready_queue"),
+                                "unfused": lambda: call("unfused"), "mm_only": lambda: call("mm_only")},
+                               max(args.steps, 60), dist, stream)
+        line = {k: round(aggregate(v, float(cfg.flops), dist)[0], 1) for k, v in med.items()}
+        line["unit"] = "TFLOP/s"
+        line["config"] = f"{cfg.R} x ({cfg.H},{cfg.K}) shards, B ({cfg.N},{cfg.K}), cb={cfg.cb}"
+        out[name] = line
+        del shards, B, C, a
+    return out
 
 
 def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
@@ -365,45 +434,81 @@ def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
 
 
 def bench_e2e(cfg, shards_h, B_h, a, progress, ws, order, delay, dev, stream, dist, args):
-    """The public call with host buffers: H2D of the shards and B from pinned memory, the fused
-    call (synchronous), D2H of C into pinned memory -- all inside the timed region."""
+    """The public call with host buffers, pipelined the way an application streams batches:
+    every step copies its shards and B from pinned host memory (H2D stream), runs the fused
+    call on them (compute stream), and copies C back to pinned host memory (D2H stream).
+    Two device buffer sets let step i+1's inputs and step i-1's result move while step i
+    computes; the timed region covers `steps` complete steps (first H2D to last D2H)."""
     import torch
 
     import tile_gather_comm_gb300 as tgc
 
     hs = [s.pin_memory() for s in shards_h]
     hB = B_h.pin_memory()
-    hC = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16).pin_memory()
-    ds = [torch.empty_like(s, device=dev) for s in hs]
-    dB = torch.empty_like(hB, device=dev)
-    dC = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)
+    hC = [torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    sets = []
+    for _ in range(2):
+        sets.append(([torch.empty_like(s, device=dev) for s in hs], torch.empty_like(hB, device=dev),
+                     torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)))
     h2d = sum(s.numel() * 2 for s in hs) + hB.numel() * 2
-    d2h = hC.numel() * 2
+    d2h = cfg.M * cfg.N * 2
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     epoch = [10_000_000]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_out:
+        e.record(s_out)
 
-    def step():
-        for d, h in zip(ds, hs):
-            d.copy_(h, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
+    def step(i):
+        k = i % 2
+        ds, dB, dC = sets[k]
+        s_in.wait_event(ev_done[k])          # the set's previous kernel has consumed its inputs
+        with torch.cuda.stream(s_in):
+            for d, h in zip(ds, hs):
+                d.copy_(h, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+        ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        stream.wait_event(ev_out[k])         # the set's previous result has been copied out
         epoch[0] += 1
         tgc.tgc_ag_matmul_ex(ds, dB, dC, a, cfg.cb, progress=progress, epoch=epoch[0], workspace=ws,
-                             order=order, delay_ns=delay, sync=True, stream=stream)
-        hC.copy_(dC, non_blocking=True)
-        stream.synchronize()
+                             order=order, delay_ns=delay, stream=stream)
+        ev_done[k].record(stream)
+        s_out.wait_event(ev_done[k])
+        with torch.cuda.stream(s_out):
+            hC[k].copy_(dC, non_blocking=True)
+        ev_out[k].record(s_out)
 
-    steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        step()
+    steps = max(4, min(args.steps, 20))
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
     dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    for i in range(steps):
+        step(i)
+    torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / steps
     dist.barrier()
+    # raw pinned-copy rates on this box, for context
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    sets[0][1].copy_(hB, non_blocking=True)
+    e1.record(s_in)
+    torch.cuda.synchronize()
+    h2d_gbs = hB.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) * 1e-9
+    e0.record(s_out)
+    hC[0].copy_(sets[0][2], non_blocking=True)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    d2h_gbs = d2h / (e0.elapsed_time(e1) * 1e-3) * 1e-9
     val, ms_max = aggregate(ms, float(cfg.flops), dist)
     return {"value": round(val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms_max, 3), "steps": steps,
-            "call": "tgc_ag_matmul_ex(sync=1) with pinned-host H2D inputs and D2H of C"}
+            "call": "tgc_ag_matmul_ex on a compute stream; pinned H2D and D2H on their own streams, "
+                    "two device buffer sets (steps overlap)",
+            "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1)}
 
 
 def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):

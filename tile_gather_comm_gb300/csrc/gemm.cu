@@ -63,6 +63,20 @@ namespace tgc {
 #ifndef TGC_COPY_SLOTS
 #define TGC_COPY_SLOTS 4         // staging slots of the copy producer
 #endif
+// L2 policies: 0 = default, 1 = evict_first, 2 = evict_last, 3 = evict_normal
+#ifndef TGC_COPY_HINT
+#define TGC_COPY_HINT 0          // producer's bulk loads of the shards and stores into `a`
+#endif
+#ifndef TGC_A_HINT
+#define TGC_A_HINT 0             // tile loads of A
+#endif
+#ifndef TGC_B_HINT
+#define TGC_B_HINT 0             // tile loads of B
+#endif
+
+__device__ __forceinline__ uint64_t make_policy(int kind) {
+    return kind == 1 ? policy_evict_first() : kind == 2 ? policy_evict_last() : policy_evict_normal();
+}
 
 constexpr int kThreads = 256;
 constexpr int kSlots = TGC_COPY_SLOTS;
@@ -252,6 +266,7 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     uint64_t wait_ns = 0, waited_tiles = 0;
     // completion of every stage is counted on the even CTA's full barrier
     const uint32_t full0 = CG == 2 ? mapa_shared(smem_addr(full), 0) : smem_addr(full);
+    const uint64_t polA = make_policy(TGC_A_HINT), polB = make_policy(TGC_B_HINT);
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>()) {
         TilePos tp = tile_at(p, t);
         if (tp.ring_idx >= 0) {
@@ -290,13 +305,17 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
                 if (!mbar_wait(&empty[s], ph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
                 if (CG == 1) {
                     mbar_arrive_expect_tx(&full[s], C::kStageTx);
-                    tma_load_2d(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow);
-                    tma_load_2d(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb);
+                    if (TGC_A_HINT) tma_load_2d_hint(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow, polA);
+                    else tma_load_2d(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow);
+                    if (TGC_B_HINT) tma_load_2d_hint(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb, polB);
+                    else tma_load_2d(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb);
                 } else {
                     if (crank == 0) mbar_arrive_expect_tx(&full[s], C::kStageTx);  // both CTAs' bytes
                     const uint32_t bar = full0 + s * 8u;
-                    tma_load_2d_pair(sA + s * C::kAStage, mapA, bar, kb * kBK, arow);
-                    tma_load_2d_pair(sB + s * C::kBStage, tmB, bar, kb * kBK, nb);
+                    if (TGC_A_HINT) tma_load_2d_pair_hint(sA + s * C::kAStage, mapA, bar, kb * kBK, arow, polA);
+                    else tma_load_2d_pair(sA + s * C::kAStage, mapA, bar, kb * kBK, arow);
+                    if (TGC_B_HINT) tma_load_2d_pair_hint(sB + s * C::kBStage, tmB, bar, kb * kBK, nb, polB);
+                    else tma_load_2d_pair(sB + s * C::kBStage, tmB, bar, kb * kBK, nb);
                 }
             }
         }
@@ -507,6 +526,7 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
     uint32_t cur_off = 0, cur_ring = 0;
     bool have_cur = false, nomore = false, ok = true;
     const uint64_t t_first = p.trace != nullptr ? globaltimer_ns() : 0;
+    const uint64_t pol = make_policy(TGC_COPY_HINT);
     for (;;) {
         // issue loads while a slot is free (its previous store has read it)
         while (tail - head < (uint32_t)kSlots) {
@@ -528,7 +548,8 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
             slot_piece[slot] = cur_ring;
             slot_off[slot] = cur_off;
             mbar_arrive_expect_tx(&slotbar[slot], nb);
-            bulk_g2s(sSlot + slot * kSlotBytes, cur.src + cur_off, nb, &slotbar[slot]);
+            if (TGC_COPY_HINT) bulk_g2s_hint(sSlot + slot * kSlotBytes, cur.src + cur_off, nb, &slotbar[slot], pol);
+            else bulk_g2s(sSlot + slot * kSlotBytes, cur.src + cur_off, nb, &slotbar[slot]);
             cur_off += nb;
             if (cur_off == cur.bytes) have_cur = false;
             ++tail;
@@ -554,7 +575,8 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
             const uint32_t off = slot_off[slot];
             const uint32_t left = pc.bytes - off;
             const uint32_t nb = left < (uint32_t)kSlotBytes ? left : (uint32_t)kSlotBytes;
-            bulk_s2g(pc.dst + off, sSlot + slot * kSlotBytes, nb);
+            if (TGC_COPY_HINT) bulk_s2g_hint(pc.dst + off, sSlot + slot * kSlotBytes, nb, pol);
+            else bulk_s2g(pc.dst + off, sSlot + slot * kSlotBytes, nb);
             bulk_commit();
             ++head;
             if (off + nb == pc.bytes) ring_last_store[pr] = head;  // stores [0, head) cover this piece
