@@ -261,16 +261,20 @@ typedef struct tgc_ag_matmul_args {
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 
-/* Per-CTA trace words (all times in ns of %globaltimer). */
-#define TGC_TRACE_WORDS 8
-#define TGC_TRACE_START 0       /* CTA start                                   */
-#define TGC_TRACE_WAIT_NS 1     /* total time the tile scheduler spent on flags */
-#define TGC_TRACE_WAITED_TILES 2 /* tiles that found a flag not yet set         */
-#define TGC_TRACE_COPY_FIRST 3  /* producer: first piece handed out            */
-#define TGC_TRACE_COPY_LAST 4   /* producer: last piece of this CTA retired    */
-#define TGC_TRACE_PIECES 5      /* producer: pieces copied by this CTA         */
-#define TGC_TRACE_END 6         /* epilogue: last tile of this CTA stored      */
-#define TGC_TRACE_TILES 7       /* tiles computed by this CTA                  */
+/* Per-CTA trace words (times in ns of %globaltimer). */
+#define TGC_TRACE_WORDS 16
+#define TGC_TRACE_START 0        /* CTA start                                        */
+#define TGC_TRACE_WAIT_NS 1      /* tile scheduler: time spent waiting on flags/ring */
+#define TGC_TRACE_WAITED_TILES 2 /* tiles that found their data not yet published    */
+#define TGC_TRACE_COPY_FIRST 3   /* producer: first piece handed out                 */
+#define TGC_TRACE_COPY_LAST 4    /* producer: last piece of this CTA retired         */
+#define TGC_TRACE_PIECES 5       /* producer: pieces copied by this CTA              */
+#define TGC_TRACE_END 6          /* epilogue: last tile of this CTA stored           */
+#define TGC_TRACE_TILES 7        /* tiles computed by this CTA                       */
+#define TGC_TRACE_MMA_STAGE_NS 8 /* MMA issuer: time waiting for operand stages     */
+#define TGC_TRACE_MMA_ACC_NS 9   /* MMA issuer: time waiting for a free accumulator  */
+#define TGC_TRACE_EPI_WAIT_NS 10 /* epilogue (first warp): time waiting for results  */
+#define TGC_TRACE_LOAD_STALL_NS 11 /* TMA issuer: time waiting for free stages       */
 
 /*
  * tgc_ag_matmul_noalloc -- the fused AllGather-MatMul of tgc_ag_matmul with

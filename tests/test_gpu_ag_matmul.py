@@ -214,3 +214,53 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     run.C.zero_()
     run(mode="fused", pivot="ready_queue", **kw)
     assert torch.equal(run.C, C_fused), "ready-queue order differs"
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("R,H,K,N,cb", [
+    (64, 16, 64, 64, 16),      # the maximum rank count, one block per rank
+    (64, 8, 128, 24, 4),       # 64 ranks, blocks smaller than a tile, tiles straddling 32 ranks
+    (1, 512, 64, 256, 64),     # a single rank: every tile local, nothing to wait for
+    (2, 1024, 8, 8, 1),        # K = 8 (one 16-byte row), N = 8, one-row blocks: 2048 flags
+    (4, 2048, 64, 264, 8),     # 1024 blocks of 8 rows, N not a multiple of the tile
+])
+def test_edge_shapes_full(R, H, K, N, cb):
+    cfg, shards, B = _custom(R, H, K, N, cb, seed=R + H + K)
+    C_ref, a_ref = _oracle_full(shards, B)
+    run = Run(cfg, shards, B)
+    for mode, pivot, rank in (("fused", "page", 0), ("fused", "ready_queue", R - 1), ("fused", "shard", R // 2),
+                              ("unfused", "page", 0)):
+        run.C.zero_()
+        run.a.view(torch.int16).fill_(-1)
+        run(mode=mode, pivot=pivot, rank=rank)
+        assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank}")
+        assert np.array_equal(bits16(run.a), a_ref)
+
+
+def test_explicit_grid_sizes_give_identical_results():
+    """Fewer persistent clusters than SMs (down to one) change only the schedule."""
+    cfg, shards, B = _custom(4, 256, 128, 512, 64, seed=11)
+    run = Run(cfg, shards, B)
+    run(mode="unfused")
+    ref = run.C.clone()
+    for grid in (2, 6, 30):
+        for pivot in ("page", "ready_queue"):
+            run.C.zero_()
+            run(grid=grid, pivot=pivot)
+            assert torch.equal(run.C, ref), (grid, pivot)
+
+
+def test_trace_records_every_cta():
+    cfg, shards, B = _custom(4, 512, 256, 1024, 64, seed=12)
+    run = Run(cfg, shards, B)
+    trace = torch.zeros(152 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+    run(trace=trace)
+    t = trace.view(-1, _lib.TRACE_WORDS).cpu()
+    used = t[t[:, _lib.TRACE["start"]] > 0]
+    assert used.shape[0] >= 2
+    # both CTAs of a pair count each 256 x 256 tile they share
+    assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
+    assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
+    assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])

@@ -131,3 +131,19 @@ def test_progress_release(H, W, chunk_rows, D0):
     assert _bytes(dst) == oracle.tgather([s.numpy() for s in srcs]).tobytes()
     assert torch.all(progress == 7)
     assert torch.all(counters == 0)
+
+
+@pytest.mark.parametrize("nranks,shape,dtype", [
+    (64, (1, 1, 1, 3, 5), torch.int32),       # the maximum rank count
+    (64, (2, 1, 1, 17, 128), torch.float16),
+    (1, (1, 1, 1, 1, 1), torch.uint8),        # one element
+    (3, (4, 3, 2, 1, 9), torch.float64),      # many slabs, one row each
+])
+def test_edge_counts(nranks, shape, dtype):
+    es = torch.empty((), dtype=dtype).element_size()
+    g = torch.Generator().manual_seed(nranks + es)
+    srcs = [torch.randint(0, 256, shape + (es,), generator=g, dtype=torch.uint8).view(dtype).reshape(shape)
+            for _ in range(nranks)]
+    dst = torch.zeros(shape[:3] + (nranks * shape[3], shape[4]), dtype=dtype, device=DEV)
+    tgc.tgc_tgather(dst, [s.to(DEV) for s in srcs])
+    assert _bytes(dst) == _bytes(torch.cat(srcs, dim=3))

@@ -145,8 +145,22 @@ struct GemmParams {
 };
 
 // Trace word indices (mirrors TGC_TRACE_* in tgc.h).
-constexpr int kTraceWords = 8;
-enum : int { kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles };
+constexpr int kTraceWords = 16;
+enum : int {
+    kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles,
+    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs
+};
+
+// mbar_wait that adds the time it blocked to *acc (only when tracing).
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, int *status, uint64_t timeout_ns,
+                                                bool trace, uint64_t *acc) {
+    if (!trace) return mbar_wait(bar, parity, status, timeout_ns);
+    if (mbar_try_wait(smem_addr(bar), parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const bool ok = mbar_wait(bar, parity, status, timeout_ns);
+    *acc += globaltimer_ns() - t0;
+    return ok;
+}
 
 // ---------------------------------------------------------------- flag wait
 
@@ -263,7 +277,7 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     using C = Cfg<CG, FUSED>;
     uint32_t it = 0;
     bool ok = true;
-    uint64_t wait_ns = 0, waited_tiles = 0;
+    uint64_t wait_ns = 0, waited_tiles = 0, load_stall_ns = 0;
     // completion of every stage is counted on the even CTA's full barrier
     const uint32_t full0 = CG == 2 ? mapa_shared(smem_addr(full), 0) : smem_addr(full);
     const uint64_t polA = make_policy(TGC_A_HINT), polB = make_policy(TGC_B_HINT);
@@ -302,7 +316,8 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         if (lane == 0) {
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                 const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+                if (!mbar_wait_timed(&empty[s], ph ^ 1u, p.status, p.mbar_timeout_ns, p.trace != nullptr,
+                                     &load_stall_ns)) { ok = false; break; }
                 if (CG == 1) {
                     mbar_arrive_expect_tx(&full[s], C::kStageTx);
                     if (TGC_A_HINT) tma_load_2d_hint(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow, polA);
@@ -325,6 +340,7 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     if (p.trace != nullptr && lane == 0) {
         p.trace[blockIdx.x * kTraceWords + kTrWaitNs] = wait_ns;
         p.trace[blockIdx.x * kTraceWords + kTrWaitedTiles] = waited_tiles;
+        p.trace[blockIdx.x * kTraceWords + kTrLoadStallNs] = load_stall_ns;
     }
     if (!ok && lane == 0) {
         if (CG == 1 || crank == 0) {
@@ -350,15 +366,17 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
     if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
+        uint64_t stage_ns = 0, acc_ns = 0;
+        const bool tr = p.trace != nullptr;
         const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
         for (int t = cluster_id<CG>(); t < p.sched.num_tiles && ok; t += num_clusters<CG>(), ++tc) {
             const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-            if (!mbar_wait(&tempty[acc], aph ^ 1u, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+            if (!mbar_wait_timed(&tempty[acc], aph ^ 1u, p.status, p.mbar_timeout_ns, tr, &acc_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + acc * (uint32_t)kBN;
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                 const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
-                if (!mbar_wait(&full[s], ph, p.status, p.mbar_timeout_ns)) { ok = false; break; }
+                if (!mbar_wait_timed(&full[s], ph, p.status, p.mbar_timeout_ns, tr, &stage_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t ad = make_sw128_kmajor_desc(a_base + s * C::kAStage);
                 const uint64_t bd = make_sw128_kmajor_desc(b_base + s * C::kBStage);
@@ -381,6 +399,10 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
         if (CG == 1) mma_commit(drain);  // every MMA issued above has completed once this arrives
         else mma_commit_pair_mc(drain, (uint16_t)0x1);
         mbar_drain_wait(drain, 0, kDrainTimeoutNs);
+        if (tr) {
+            p.trace[blockIdx.x * kTraceWords + kTrMmaStageNs] = stage_ns;
+            p.trace[blockIdx.x * kTraceWords + kTrMmaAccNs] = acc_ns;
+        }
     }
     __syncwarp();
 }
@@ -394,11 +416,13 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
     // the accumulator is released on the even CTA's barrier
     const uint32_t tempty0 = CG == 2 ? mapa_shared(smem_addr(tempty), 0) : smem_addr(tempty);
     uint32_t tc = 0;
+    uint64_t epi_ns = 0;
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>(), ++tc) {
         TilePos tp = tile_at(p, t);
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&tfull[acc], aph, p.status, p.mbar_timeout_ns);
+        if (lane == 0)
+            ok = mbar_wait_timed(&tfull[acc], aph, p.status, p.mbar_timeout_ns, p.trace != nullptr, &epi_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform: tcgen05.ld is .sync.aligned
         if (!ok) break;
         if (tp.ring_idx >= 0) {  // already published: the loads of this tile waited for it
@@ -442,6 +466,7 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
     if (p.trace != nullptr && warp == 4 && lane == 0) {
         p.trace[blockIdx.x * kTraceWords + kTrEnd] = globaltimer_ns();
         p.trace[blockIdx.x * kTraceWords + kTrTiles] = tc;
+        p.trace[blockIdx.x * kTraceWords + kTrEpiWaitNs] = epi_ns;
     }
 }
 

@@ -45,6 +45,12 @@ namespace tgc {
 #ifndef TGC_TG_PDL
 #define TGC_TG_PDL 1         // programmatic dependent launch for the flat kernel
 #endif
+#ifndef TGC_TG_MIN_SHARE
+#define TGC_TG_MIN_SHARE 4096  // smallest byte share per CTA of the flat kernel
+#endif
+#ifndef TGC_TG_CTAS_PER_SM
+#define TGC_TG_CTAS_PER_SM 8   // CTAs per SM in one wave
+#endif
 
 constexpr int kTGThreads = TGC_TG_THREADS;
 constexpr int kTGUnroll = TGC_TG_UNROLL;
@@ -255,12 +261,12 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int64_t slots = (int64_t)sm_count(dev) * (2048 / kTGThreads);
+    const int64_t slots = (int64_t)sm_count(dev) * TGC_TG_CTAS_PER_SM;
 
     if (TGC_TG_FLAT && L.progress == nullptr) {
-        // equal 16-byte-aligned shares over one full wave (or fewer CTAs for small copies)
+        // equal 16-byte-aligned shares over one full wave (fewer CTAs only for small copies)
         const int64_t total = L.nslab * L.nranks * L.run_bytes;
-        const int64_t min_share = (int64_t)kTGThreads * kTGUnroll * 16;  // 16 KiB
+        const int64_t min_share = TGC_TG_MIN_SHARE;
         int64_t grid = (total + min_share - 1) / min_share;
         if (grid > slots) grid = slots;
         if (grid < 1) grid = 1;
