@@ -155,9 +155,17 @@ int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *
                   cudaStream_t stream);
 
 typedef enum tgc_mode {
-    TGC_MODE_FUSED = 0,   /* one kernel: copy blocks into a_out + flag-waiting GEMM */
-    TGC_MODE_UNFUSED = 1, /* tgather kernel into a_out, then the GEMM kernel on a_out */
-    TGC_MODE_MM_ONLY = 2  /* GEMM kernel on a_out as it is (every block taken as ready) */
+    TGC_MODE_FUSED = 0,    /* one kernel: copy blocks into a_out + flag-waiting GEMM */
+    TGC_MODE_UNFUSED = 1,  /* tgather kernel into a_out, then the GEMM kernel on a_out */
+    TGC_MODE_MM_ONLY = 2,  /* GEMM kernel on a_out as it is (every block taken as ready) */
+    TGC_MODE_FUSED_CE = 3  /* copy engines fill a_out block by block on a library-owned
+                              side stream, each block followed by a stream write of its
+                              progress flag; the flag-waiting GEMM kernel runs at the same
+                              time with no producer warps ([AGM] section
+                              数据搬运与细粒度同步: the backend stream copies every
+                              (src_rank, split_id) chunk and then stream_write_value32's
+                              its progress entry).  delay_ns is ignored and READY_QUEUE
+                              behaves as PAGE in this mode. */
 } tgc_mode;
 
 /*

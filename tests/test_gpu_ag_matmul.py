@@ -71,7 +71,7 @@ def _custom(R, H, K, N, cb, seed=0, sigma=1.0):
 # ----------------------------------------------------------------------------- small, full compare
 
 
-@pytest.mark.parametrize("mode", ["fused", "unfused"])
+@pytest.mark.parametrize("mode", ["fused", "unfused", "fused_ce"])
 @pytest.mark.parametrize("pivot", ["page", "shard", "none", "ready_queue"])
 def test_tiny_all_ranks(mode, pivot):
     cfg, shards, B = _inputs("tiny")
@@ -83,7 +83,7 @@ def test_tiny_all_ranks(mode, pivot):
         run(mode=mode, pivot=pivot, rank=rank)
         assert_within_tol(run.C, C_ref, f"tiny {mode} {pivot} rank {rank}")
         assert np.array_equal(bits16(run.a), a_ref)
-        if mode == "fused":
+        if mode in ("fused", "fused_ce"):
             assert torch.all(run.progress == run.epoch)
 
 
@@ -94,7 +94,7 @@ def test_ragged_shapes_full(R, H, K, N, cb):
     cfg, shards, B = _custom(R, H, K, N, cb, seed=R * H)
     C_ref, a_ref = _oracle_full(shards, B)
     run = Run(cfg, shards, B)
-    for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue")):
+    for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue"), ("fused_ce", "page")):
         for rank in sorted({0, R - 1}):
             run.C.zero_()
             run(mode=mode, rank=rank, pivot=pivot)
@@ -181,6 +181,11 @@ def test_withheld_block_times_out_and_context_survives():
     assert rc == _lib.TGC_ERR_TIMEOUT
     run.ws.zero_()
     run.progress.zero_()
+    rc = run(order=order, spin_timeout_ns=2_000_000, check=False, mode="fused_ce")
+    assert rc == _lib.TGC_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    run.ws.zero_()
+    run.progress.zero_()
     run.epoch = 0
     run()
     C_ref, _ = _oracle_full(shards, B)
@@ -214,6 +219,11 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     run.C.zero_()
     run(mode="fused", pivot="ready_queue", **kw)
     assert torch.equal(run.C, C_fused), "ready-queue order differs"
+    run.C.zero_()
+    run.a.view(torch.int16).fill_(-1)
+    run(mode="fused_ce", **{k: v for k, v in kw.items() if k == "order"})
+    assert torch.equal(run.C, C_fused), "copy-engine producer differs"
+    assert torch.equal(run.a, torch.cat(run.shards))
 
 
 # ----------------------------------------------------------------------------- edge cases

@@ -26,7 +26,7 @@ TGC_ERR_WORKSPACE = -8
 TGC_ERR_TOO_LARGE = -9
 NOALLOC_MAX_BLOCKS = 2048
 
-MODES = {"fused": 0, "unfused": 1, "mm_only": 2}
+MODES = {"fused": 0, "unfused": 1, "mm_only": 2, "fused_ce": 3}
 PIVOTS = {"page": 0, "shard": 1, "none": 2, "ready_queue": 3}
 DTYPES = {
     torch.uint8: 0, torch.int8: 1, torch.float16: 2, torch.bfloat16: 3,

@@ -7,6 +7,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -142,14 +144,16 @@ static int tgather_impl(const tgc_tgather_args &a) {
 int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.nranks <= 0 || a.nranks > TGC_MAX_RANKS) return TGC_ERR_INVALID_ARG;
     if (a.M < 0 || a.K < 0 || a.N < 0) return TGC_ERR_INVALID_ARG;
-    if (a.mode != TGC_MODE_FUSED && a.mode != TGC_MODE_UNFUSED && a.mode != TGC_MODE_MM_ONLY)
+    if (a.mode != TGC_MODE_FUSED && a.mode != TGC_MODE_UNFUSED && a.mode != TGC_MODE_MM_ONLY &&
+        a.mode != TGC_MODE_FUSED_CE)
         return TGC_ERR_INVALID_ARG;
+    const bool flagged = a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE;
     if (a.pivot != TGC_PIVOT_PAGE && a.pivot != TGC_PIVOT_SHARD && a.pivot != TGC_PIVOT_NONE &&
         a.pivot != TGC_PIVOT_READY_QUEUE)
         return TGC_ERR_INVALID_ARG;
     if (a.M % a.nranks != 0) return TGC_ERR_INVALID_ARG;
     const int64_t rows_per_rank = a.M / a.nranks;
-    if (a.mode == TGC_MODE_FUSED) {
+    if (flagged) {
         if (a.comm_block_rows <= 0) return TGC_ERR_INVALID_ARG;
         if (rows_per_rank % a.comm_block_rows != 0) return TGC_ERR_INVALID_ARG;
     }
@@ -159,7 +163,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 31))
         return TGC_ERR_INVALID_ARG;
     out.rows_per_rank = rows_per_rank;
-    out.nblocks = a.mode == TGC_MODE_FUSED ? a.M / a.comm_block_rows : 0;
+    out.nblocks = flagged ? a.M / a.comm_block_rows : 0;
     if (a.M == 0 || a.N == 0) return 1;  // nothing to do
     if (a.K == 0) return TGC_ERR_INVALID_ARG;
     if (a.K % 8 != 0 || a.N % 8 != 0) return TGC_ERR_ALIGN;
@@ -172,7 +176,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
             if (!aligned(a.a_shards[r], 16)) return TGC_ERR_ALIGN;
         }
     }
-    if (a.mode == TGC_MODE_FUSED) {
+    if (flagged) {
         if (out.nblocks >= (int64_t(1) << 24)) return TGC_ERR_INVALID_ARG;
         if (a.progress == nullptr || !aligned(a.progress, 4)) return TGC_ERR_INVALID_ARG;
         if (a.workspace == nullptr) return TGC_ERR_WORKSPACE;
@@ -194,6 +198,108 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;
     if (a.trace != nullptr && !aligned(a.trace, 8)) return TGC_ERR_ALIGN;
     return 0;
+}
+
+// ------------------------------------------------------------------ copy-engine producer
+
+using WriteValue32Fn = PFN_cuStreamWriteValue32_v11070;
+
+static WriteValue32Fn write_value32_fn() {
+    static WriteValue32Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &f, 11070, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<WriteValue32Fn>(f);
+    });
+    return fn;
+}
+
+#ifndef TGC_CE_STREAMS
+#define TGC_CE_STREAMS 4  // side streams of the copy-engine producer (blocks round-robin)
+#endif
+constexpr int kCeStreams = TGC_CE_STREAMS;
+
+// Per-device side streams and events of the copy-engine producer.
+struct CeState {
+    std::mutex mu;
+    cudaStream_t side[kCeStreams] = {};
+    cudaEvent_t start = nullptr;
+    cudaEvent_t done[kCeStreams] = {};
+    bool ready = false;
+};
+
+static int ce_state(int device, CeState **out) {
+    constexpr int kMaxDevices = 64;
+    static CeState states[kMaxDevices];
+    if (device < 0 || device >= kMaxDevices) return TGC_ERR_INVALID_ARG;
+    CeState &st = states[device];
+    std::lock_guard<std::mutex> lock(st.mu);
+    if (!st.ready) {
+        int lo = 0, hi = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        for (int i = 0; i < kCeStreams && e == cudaSuccess; ++i) {
+            e = cudaStreamCreateWithPriority(&st.side[i], cudaStreamNonBlocking, hi);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.done[i], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.start, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+        st.ready = true;
+    }
+    *out = &st;
+    return TGC_OK;
+}
+
+// The gather of FUSED_CE: on the side streams, after everything enqueued on
+// `stream` so far, one device-to-device copy per comm block in release order
+// (blocks dealt round-robin to the side streams, so several copy engines run
+// at once), each followed by a stream write of `epoch` into its progress entry
+// (the write's default memory barrier orders the block's bytes before the
+// flag).  `launch` enqueues the consumer kernel on `stream`; `stream` then
+// waits for every side stream, so the call completes only when `a_out` is whole.
+template <class LaunchFn>
+static int ce_fused(const tgc_ag_matmul_args &a, const AGCheck &chk, int64_t first_block, LaunchFn launch) {
+    auto wv = write_value32_fn();
+    if (wv == nullptr) return TGC_ERR_CUDA;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    CeState *st = nullptr;
+    int rc = ce_state(dev, &st);
+    if (rc != TGC_OK) return rc;
+    std::lock_guard<std::mutex> lock(st->mu);
+    e = cudaEventRecord(st->start, a.stream);
+    for (int i = 0; i < kCeStreams && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(st->side[i], st->start, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t S = chk.rows_per_rank / a.comm_block_rows;
+    const int64_t nb = chk.nblocks;
+    const int local_b0 = (int)(a.rank * S), local_b1 = (int)((a.rank + 1) * S);
+    const int64_t n = a.order != nullptr ? a.n_order : nb;
+    const size_t block_bytes = (size_t)a.comm_block_rows * (size_t)a.K * 2;
+    for (int64_t pos = 0; pos < n; ++pos) {
+        const int64_t c = a.order != nullptr ? a.order[pos]
+                                            : default_release_block((int)pos, (int)nb, (int)first_block, local_b0,
+                                                                    local_b1);
+        const int64_t r = c / S, sidx = c % S;
+        const uint8_t *src = static_cast<const uint8_t *>(a.a_shards[r]) + (size_t)sidx * block_bytes;
+        uint8_t *dst = static_cast<uint8_t *>(a.a_out) +
+                       ((size_t)(r * chk.rows_per_rank + sidx * a.comm_block_rows)) * (size_t)a.K * 2;
+        cudaStream_t side = st->side[pos % kCeStreams];
+        e = cudaMemcpyAsync(dst, src, block_bytes, cudaMemcpyDeviceToDevice, side);
+        if (e != cudaSuccess) return cuda_fail(e);
+        CUresult cr = wv(reinterpret_cast<CUstream>(side), reinterpret_cast<CUdeviceptr>(a.progress + c), a.epoch, 0);
+        if (cr != CUDA_SUCCESS) return TGC_ERR_CUDA;
+    }
+    for (int i = 0; i < kCeStreams && e == cudaSuccess; ++i) e = cudaEventRecord(st->done[i], st->side[i]);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rc = launch();
+    // even if the launch failed: keep stream order
+    for (int i = 0; i < kCeStreams && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(a.stream, st->done[i], 0);
+    if (rc != TGC_OK) return rc;
+    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
 
 static int ag_ex_impl(const tgc_ag_matmul_args &a) {
@@ -224,7 +330,9 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.N = a.N;
     G.cb = a.comm_block_rows;
     G.rank = a.rank;
-    G.pivot = (a.pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED) ? (int)TGC_PIVOT_NONE : (int)a.pivot;
+    G.pivot = (a.pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED)
+                  ? (a.mode == TGC_MODE_FUSED_CE ? (int)TGC_PIVOT_PAGE : (int)TGC_PIVOT_NONE)
+                  : (int)a.pivot;
     G.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
     G.grid = a.grid;
     G.timeout_ns = timeout;
@@ -233,8 +341,9 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     if (a.mode != TGC_MODE_MM_ONLY)
         for (int r = 0; r < a.nranks; ++r) G.shards[r] = a.a_shards[r];
 
-    if (a.mode == TGC_MODE_FUSED) {
+    if (a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE) {
         G.fused = true;
+        G.producer = a.mode == TGC_MODE_FUSED;
         G.progress = a.progress;
         G.epoch = a.epoch;
         G.ws_counters = reinterpret_cast<uint32_t *>(ws + wl.counters_off);
@@ -254,7 +363,14 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
             G.delay_ns = reinterpret_cast<const uint32_t *>(ws + wl.delay_off);
         }
         if (status == nullptr) return TGC_ERR_WORKSPACE;
-        rc = launch_gemm(G, st);
+        if (a.mode == TGC_MODE_FUSED_CE) {
+            const int64_t tiles_m = tile_rows_of(a.M);
+            const int64_t off = pivot_offset(G.pivot, a.rank, a.comm_block_rows, chk.rows_per_rank, kTileM,
+                                             (int)tiles_m);
+            rc = ce_fused(a, chk, off * kTileM / a.comm_block_rows, [&] { return launch_gemm(G, st); });
+        } else {
+            rc = launch_gemm(G, st);
+        }
         if (rc != TGC_OK) return rc;
     } else {
         if (a.mode == TGC_MODE_UNFUSED) {

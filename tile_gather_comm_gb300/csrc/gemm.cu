@@ -86,23 +86,23 @@ constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns 
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 
 // Per-CTA-group configuration.  CG = number of CTAs sharing one MMA tile.
-template <int CG, bool FUSED>
+template <int CG, bool SLOTS>  // SLOTS: the copy producer's staging slots share shared memory
 struct Cfg {
     static constexpr int kTileM = 128 * CG;             // output rows per (cluster) tile
     static constexpr int kRowsCta = 128;                // rows of A per CTA
     static constexpr int kHalfN = kBN / CG;             // rows of B (N) each CTA stages
     static constexpr int kAStage = kRowsCta * kBK * 2;  // 16 KiB
     static constexpr int kBStage = kHalfN * kBK * 2;    // 32 KiB alone, 16 KiB in a pair
-    static constexpr int kStages = CG == 1 ? 4 : (FUSED ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
+    static constexpr int kStages = CG == 1 ? 4 : (SLOTS ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
     static constexpr uint32_t kIdesc = make_idesc_bf16_f32(kTileM, kBN);
     static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
     static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
 };
 
-template <int CG, bool FUSED>
+template <int CG, bool SLOTS>
 constexpr int smem_bytes() {
-    return 1024 /* alignment slack */ + Cfg<CG, FUSED>::kStages * (Cfg<CG, FUSED>::kAStage + Cfg<CG, FUSED>::kBStage) +
-           (FUSED ? kSlots * kSlotBytes : 0) + 256 /* barriers + TMEM address */;
+    return 1024 /* alignment slack */ + Cfg<CG, SLOTS>::kStages * (Cfg<CG, SLOTS>::kAStage + Cfg<CG, SLOTS>::kBStage) +
+           (SLOTS ? kSlots * kSlotBytes : 0) + 256 /* barriers + TMEM address */;
 }
 static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<2, false>() <= 232448, "shared memory per CTA");
 
@@ -270,11 +270,11 @@ __device__ __forceinline__ int cluster_id() { return (int)blockIdx.x / CG; }
 template <int CG>
 __device__ __forceinline__ int num_clusters() { return (int)gridDim.x / CG; }
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint32_t crank, int lane) {
-    using C = Cfg<CG, FUSED>;
+    using C = Cfg<CG, FUSED && PROD>;
     uint32_t it = 0;
     bool ok = true;
     uint64_t wait_ns = 0, waited_tiles = 0, load_stall_ns = 0;
@@ -358,11 +358,11 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     __syncwarp();
 }
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, uint32_t crank,
                          int lane) {
-    using C = Cfg<CG, FUSED>;
+    using C = Cfg<CG, FUSED && PROD>;
     if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
@@ -407,10 +407,10 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
     __syncwarp();
 }
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                               uint32_t crank, int warp, int lane) {
-    using C = Cfg<CG, FUSED>;
+    using C = Cfg<CG, FUSED && PROD>;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     // the accumulator is released on the even CTA's barrier
@@ -645,18 +645,18 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 __global__ void __launch_bounds__(kThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-    using C = Cfg<CG, FUSED>;
+    using C = Cfg<CG, FUSED && PROD>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kAStage;
     uint8_t *sSlot = sB + C::kStages * C::kBStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (FUSED ? kSlots * kSlotBytes : 0));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (FUSED && PROD ? kSlots * kSlotBytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
@@ -691,13 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        role_tma<CG, FUSED>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
+        role_tma<CG, FUSED, PROD>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
-        role_mma<CG, FUSED>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
+        role_mma<CG, FUSED, PROD>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
     } else if (warp == 2) {
-        if (FUSED) role_copy(p, sSlot, slotbar, lane);
+        if (FUSED && PROD) role_copy(p, sSlot, slotbar, lane);
     } else if (warp >= 4) {
-        role_epilogue<CG, FUSED>(p, tfull, tempty, tmem_base, crank, warp, lane);
+        role_epilogue<CG, FUSED, PROD>(p, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
     // In a pair, the even CTA's MMAs read the odd CTA's shared memory and write
@@ -755,19 +755,19 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t col
 // CTAs that share one MMA tile in the launched kernels.
 constexpr int kCG = 2;
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 static int set_smem_attr() {
     static cudaError_t err = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes<CG, FUSED>());
+        err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem_bytes<CG, FUSED && PROD>());
     });
     return err == cudaSuccess ? TGC_OK : cuda_fail(err);
 }
 
 // Persistent clusters that can be resident at once (one CTA per SM).
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 static int max_clusters(int sms) {
     if (CG == 1) return sms;
     static int cached = 0;
@@ -781,21 +781,21 @@ static int max_clusters(int sms) {
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes<CG, FUSED>();
+        cfg.dynamicSmemBytes = smem_bytes<CG, FUSED && PROD>();
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED, PROD>, &cfg) != cudaSuccess || n <= 0)
             n = sms / CG;
         cached = n;
     });
     return cached;
 }
 
-template <int CG, bool FUSED>
+template <int CG, bool FUSED, bool PROD>
 static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const GemmParams &p,
                   int nclusters, cudaStream_t stream) {
-    int rc = set_smem_attr<CG, FUSED>();
+    int rc = set_smem_attr<CG, FUSED, PROD>();
     if (rc != TGC_OK) return rc;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
@@ -805,11 +805,11 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CG, FUSED>();
+    cfg.dynamicSmemBytes = smem_bytes<CG, FUSED && PROD>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED>, tmA, tmL, tmB, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD>, tmA, tmL, tmB, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
@@ -868,7 +868,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.tile_m = C::kTileM;
         p.rowcnt = L.ws_rowcnt;
         p.ring = L.ws_ring;
-        if (L.pivot == TGC_PIVOT_READY_QUEUE) {
+        if (L.pivot == TGC_PIVOT_READY_QUEUE && L.producer) {
             p.rq = 1;
             p.sched.pivot_off = 0;
             // tile rows lying entirely inside [local_row0, local_row1)
@@ -887,14 +887,18 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
 
     // persistent clusters: every SM busy; for the plain GEMM no more clusters than tiles
     // (the shared-memory attribute must be set before the occupancy query)
-    int rc = L.fused ? set_smem_attr<kCG, true>() : set_smem_attr<kCG, false>();
+    const int variant = !L.fused ? 0 : (L.producer ? 1 : 2);
+    int rc = variant == 0 ? set_smem_attr<kCG, false, false>()
+           : variant == 1 ? set_smem_attr<kCG, true, true>() : set_smem_attr<kCG, true, false>();
     if (rc != TGC_OK) return rc;
-    int nclusters = L.fused ? max_clusters<kCG, true>(sms) : max_clusters<kCG, false>(sms);
+    int nclusters = variant == 0 ? max_clusters<kCG, false, false>(sms)
+                  : variant == 1 ? max_clusters<kCG, true, true>(sms) : max_clusters<kCG, true, false>(sms);
     if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
     if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
     if (nclusters < 1) nclusters = 1;
-    return L.fused ? launch<kCG, true>(tmA, tmL, tmB, p, nclusters, stream)
-                   : launch<kCG, false>(tmA, tmL, tmB, p, nclusters, stream);
+    return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, p, nclusters, stream)
+         : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, p, nclusters, stream)
+                        : launch<kCG, true, false>(tmA, tmL, tmB, p, nclusters, stream);
 }
 
 }  // namespace tgc

@@ -36,7 +36,8 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream);
 
 // Launch one of the GEMM kernels; arguments already validated.
 struct GemmLaunch {
-    bool fused;
+    bool fused;        // tiles wait on progress flags
+    bool producer;     // (fused) the kernel's own warps copy the blocks
     const void *shards[TGC_MAX_RANKS];
     int nranks;
     const void *B;
