@@ -86,6 +86,29 @@ int tgc_tgather(void *dst, const void *const *srcs, int nranks,
                 tgc_dtype dtype, cudaStream_t stream);
 
 /*
+ * tgc_tgather_strided -- the same gather on strided views ([TG] §7.3: every
+ * source is a view with one shape and one stride, shared by all sources;
+ * §8.1: GlobalTensor<T, Shape<5>, Stride, Layout::ND>):
+ *     dst[d0, d1, d2, r*H + i, j] = srcs[r][d0, d1, d2, i, j]
+ * Element (d0,d1,d2,i,j) of a source lives at
+ *     srcs[r] + es * (d0*ss[0] + d1*ss[1] + d2*ss[2] + i*ss[3] + j*ss[4]),
+ * destination element (d0,d1,d2,row,j) at
+ *     dst + es * (d0*ds[0] + d1*ds[1] + d2*ds[2] + row*ds[3] + j*ds[4]),
+ * with ss = src_strides, ds = dst_strides: host arrays of 5 element strides,
+ * each >= 0.  Only the view is written; memory between its rows and columns is
+ * left as it is.  The destination view must not overlap itself or a source
+ * (undefined otherwise).  Rows that are contiguous in both source and
+ * destination (ss[4] == ds[4] == 1) are copied with the widest vector every
+ * start address and stride allows; otherwise element by element.  Errors and
+ * the empty-input rule as tgc_tgather; a negative stride is
+ * TGC_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ */
+int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const *srcs,
+                        const int64_t *src_strides, int nranks,
+                        int64_t D0, int64_t D1, int64_t D2, int64_t H, int64_t W,
+                        tgc_dtype dtype, cudaStream_t stream);
+
+/*
  * Extended TGATHER.  Adds:
  *   dst_rows3  dst's DIM_3; 0 means nranks*H.  [TG] §7.2: it may exceed
  *              nranks*H, in which case only the first nranks*H rows of each

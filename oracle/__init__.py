@@ -46,6 +46,9 @@ def _bind(lib):
     lib.oracle_tgather.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int,
                                    i64, i64, i64, i64, i64, i64, i64]
     lib.oracle_tgather.restype = ctypes.c_int
+    lib.oracle_tgather_strided.argtypes = [vp, vp, ctypes.POINTER(vp), vp, ctypes.c_int,
+                                           i64, i64, i64, i64, i64, i64]
+    lib.oracle_tgather_strided.restype = ctypes.c_int
     lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_f32.restype = ctypes.c_float
     lib.oracle_f32_to_bf16_rne.argtypes = [ctypes.c_float]
@@ -122,6 +125,24 @@ class Oracle:
                                 dt.itemsize, rows)
         if rc != 0:
             raise ValueError(f"oracle_tgather rejected the arguments (rc={rc})")
+        return dst
+
+    def tgather_strided(self, dst: np.ndarray, srcs) -> np.ndarray:
+        """[TG] §7.3 / §8.1 strided views: writes srcs (numpy views of one shape and strides)
+        into the view ``dst`` of shape (D0,D1,D2,>=N*H,W), rows r*H+i; returns dst."""
+        n = len(srcs)
+        shape = srcs[0].shape
+        es = srcs[0].dtype.itemsize
+        if len(shape) != 5 or any(x.shape != shape or x.strides != srcs[0].strides for x in srcs):
+            raise ValueError("sources must share one 5-D shape and one stride")
+        D0, D1, D2, H, W = shape
+        sst = np.array([st // es for st in srcs[0].strides], dtype=np.int64)
+        dstr = np.array([st // es for st in dst.strides], dtype=np.int64)
+        ptrs = (ctypes.c_void_p * n)(*[x.ctypes.data for x in srcs])
+        rc = self._L.oracle_tgather_strided(dst.ctypes.data, dstr.ctypes.data, ptrs, sst.ctypes.data, n,
+                                            D0, D1, D2, H, W, es)
+        if rc != 0:
+            raise ValueError(f"oracle_tgather_strided rejected the arguments (rc={rc})")
         return dst
 
     def bf16_to_f32(self, bits: np.ndarray) -> np.ndarray:
@@ -220,6 +241,10 @@ def set_num_threads(n: int) -> None:
 
 def tgather(srcs, dst_rows3=None, dst=None):
     return _oracle().tgather(srcs, dst_rows3=dst_rows3, dst=dst)
+
+
+def tgather_strided(dst, srcs):
+    return _oracle().tgather_strided(dst, srcs)
 
 
 def bf16_to_f32(bits):

@@ -71,6 +71,43 @@ int oracle_tgather(void *dst, const void *const *srcs, int nranks,
     return 0;
 }
 
+/*
+ * Strided form of the same formula ([TG] §7.3 and §8.1: sources are
+ * GlobalTensor views with a shape and a stride, all sources sharing both).
+ * Element (d0,d1,d2,i,j) of source r lives at srcs[r] + es * sum(idx * src_strides),
+ * destination element (d0,d1,d2,r*H+i,j) at dst + es * sum(idx * dst_strides);
+ * strides are in elements and non-negative.  Empty input returns at once.
+ */
+int oracle_tgather_strided(void *dst, const int64_t *dst_strides, const void *const *srcs,
+                           const int64_t *src_strides, int nranks, int64_t D0, int64_t D1,
+                           int64_t D2, int64_t H, int64_t W, int64_t es)
+{
+    if (nranks <= 0 || es <= 0)
+        return -1;
+    for (int k = 0; k < 5; ++k)
+        if (dst_strides[k] < 0 || src_strides[k] < 0)
+            return -1;
+    if (D0 * D1 * D2 * H == 0 || W == 0)
+        return 0;
+    unsigned char *d = (unsigned char *)dst;
+    for (int r = 0; r < nranks; ++r) {
+        const unsigned char *s = (const unsigned char *)srcs[r];
+        for (int64_t d0 = 0; d0 < D0; ++d0)
+            for (int64_t d1 = 0; d1 < D1; ++d1)
+                for (int64_t d2 = 0; d2 < D2; ++d2)
+                    for (int64_t i = 0; i < H; ++i)
+                        for (int64_t j = 0; j < W; ++j) {
+                            int64_t so = d0 * src_strides[0] + d1 * src_strides[1] + d2 * src_strides[2] +
+                                         i * src_strides[3] + j * src_strides[4];
+                            int64_t row = (int64_t)r * H + i;
+                            int64_t dd = d0 * dst_strides[0] + d1 * dst_strides[1] + d2 * dst_strides[2] +
+                                         row * dst_strides[3] + j * dst_strides[4];
+                            memcpy(d + dd * es, s + so * es, (size_t)es);
+                        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* bf16 <-> fp32                                                             */
 /* ------------------------------------------------------------------------ */

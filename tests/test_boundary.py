@@ -69,6 +69,20 @@ def test_tgather_empty_returns_ok_without_touching_memory(shape):
     assert _tg(None, [None, None], 2, *shape) == _lib.TGC_OK
 
 
+def test_tgather_strided_invalid_and_empty():
+    L = _lib.lib()
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    good = (ctypes.c_int64 * 5)(1, 1, 1, 4, 1)
+    neg = (ctypes.c_int64 * 5)(1, 1, 1, 4, -1)
+    args = lambda ds, ss, H=4: (FAKE, ds, arr, ss, 2, 1, 1, 1, H, 4, 5, None)
+    assert L.tgc_tgather_strided(*args(good, neg)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_tgather_strided(*args(neg, good)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_tgather_strided(*args(None, good)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_tgather_strided(FAKE + 2, good, arr, good, 2, 1, 1, 1, 4, 4, 5, None) == _lib.TGC_ERR_ALIGN
+    # empty: returns before looking at any pointer
+    assert L.tgc_tgather_strided(None, None, arr, None, 2, 1, 1, 1, 0, 4, 5, None) == _lib.TGC_OK
+
+
 def test_tgather_ex_rejects_short_dst_and_missing_counters():
     L = _lib.lib()
     arr = (ctypes.c_void_p * 2)(FAKE, FAKE)

@@ -147,3 +147,69 @@ def test_edge_counts(nranks, shape, dtype):
     dst = torch.zeros(shape[:3] + (nranks * shape[3], shape[4]), dtype=dtype, device=DEV)
     tgc.tgc_tgather(dst, [s.to(DEV) for s in srcs])
     assert _bytes(dst) == _bytes(torch.cat(srcs, dim=3))
+
+
+# ----------------------------------------------------------------------------- strided views
+
+
+def _strided_case(case, nranks, dtype, g):
+    es = torch.empty((), dtype=dtype).element_size()
+
+    def rnd(shape):
+        return torch.randint(0, 256, shape + (es,), generator=g, dtype=torch.uint8).view(dtype).reshape(shape)
+    if case == "slices":
+        bases = [rnd((3, 2, 4, 40, 300)) for _ in range(nranks)]
+        srcs = [b[1:3, :1, 1:4, 3:35, 8:264] for b in bases]          # offset rows/cols, padded pitch
+        big = torch.zeros((2, 1, 3, nranks * 32 + 5, 300), dtype=dtype)
+        dst = big[:, :, :, 2:2 + nranks * 32, 16:272]
+    elif case == "transposed":
+        bases = [rnd((2, 1, 1, 24, 10)) for _ in range(nranks)]
+        srcs = [b.transpose(3, 4) for b in bases]                      # inner stride != 1
+        big = torch.zeros((2, 1, 1, nranks * 10, 24), dtype=dtype)
+        dst = big
+    elif case == "odd_offsets":
+        bases = [rnd((1, 1, 1, 17, 41)) for _ in range(nranks)]
+        srcs = [b[:, :, :, 1:16, 1:40] for b in bases]                # unaligned starts, odd widths
+        big = torch.zeros((1, 1, 1, nranks * 15 + 2, 45), dtype=dtype)
+        dst = big[:, :, :, 1:1 + nranks * 15, 3:42]
+    else:
+        raise ValueError(case)
+    return srcs, big, dst
+
+
+def _same_view_on_device(x):
+    """The same strided view (shape, strides, offset) over a device copy of x's whole storage."""
+    flat = torch.empty(0, dtype=x.dtype).set_(x.untyped_storage())
+    return flat.to(DEV).as_strided(x.shape, x.stride(), x.storage_offset())
+
+
+@pytest.mark.parametrize("case", ["slices", "transposed", "odd_offsets"])
+@pytest.mark.parametrize("dtype", [torch.uint8, torch.float16, torch.int32, torch.float64])
+@pytest.mark.parametrize("nranks", [1, 4])
+def test_strided_views(case, dtype, nranks):
+    g = torch.Generator().manual_seed(nranks * 31 + len(case))
+    srcs, big, dst = _strided_case(case, nranks, dtype, g)
+    ref_big = big.clone()
+    ref_dst_view = ref_big.as_strided(dst.shape, dst.stride(), dst.storage_offset())
+    oracle.tgather_strided(ref_dst_view.numpy(), [s.numpy() for s in srcs])
+    assert _bytes(ref_dst_view) == _bytes(torch.cat(srcs, dim=3))  # the oracle agrees with torch.cat (raw bits)
+    d_big = big.to(DEV)
+    d_dst = d_big.as_strided(dst.shape, dst.stride(), dst.storage_offset())
+    d_srcs = [_same_view_on_device(x) for x in srcs]
+    assert all(x.stride() == srcs[0].stride() for x in d_srcs)
+    tgc.tgc_tgather_strided(d_dst, d_srcs)
+    assert _bytes(d_big) == _bytes(ref_big)  # view written, everything around it untouched
+
+
+def test_strided_views_of_device_buffers():
+    """Sources that are strided views of device buffers (not copies)."""
+    g = torch.Generator().manual_seed(5)
+    bases = [torch.randint(-2**31, 2**31, (2, 1, 2, 50, 130), generator=g, dtype=torch.int64).to(torch.int32)
+             for _ in range(3)]
+    d_bases = [b.to(DEV) for b in bases]
+    views = [b[:, :, :, 5:45, 2:130] for b in d_bases]
+    assert views[0].stride()[3] == 130
+    dst = torch.zeros((2, 1, 2, 3 * 40, 128), dtype=torch.int32, device=DEV)
+    tgc.tgc_tgather_strided(dst, views)
+    ref = torch.cat([b[:, :, :, 5:45, 2:130] for b in bases], dim=3)
+    assert torch.equal(dst.cpu(), ref)

@@ -33,6 +33,8 @@ MUTANTS = [
      "acc += oracle_bf16_to_f32(arow[k]) * oracle_bf16_to_f32(brow[(k * 7 + 1) % K]);", ["int_exact", "f64"]),
     ("chunked_wrong_block_row", "int64_t row0 = src_rank * H + split_id * cb;",
      "int64_t row0 = src_rank * H + (S - 1 - split_id) * cb;", ["chunked"]),
+    ("strided_row_index", "int64_t row = (int64_t)r * H + i;", "int64_t row = (int64_t)r * H + (H - 1 - i);",
+     ["tg_strided"]),
     ("rows_wrong_shard", "const uint16_t *arow = a_shards[m / H] + (m % H) * K;",
      "const uint16_t *arow = a_shards[(m / H + 1) % R] + (m % H) * K;", ["rows"]),
 ]
@@ -72,13 +74,16 @@ def _run_pin(kind, o):
         pins.test_chunked_equals_gather_then_matmul(o, 0)
     elif kind == "rows":
         pins.test_rows_variant_matches_full(o)
+    elif kind == "tg_strided":
+        for case in ("slices", "transposed_w", "padded_dst"):
+            pins.test_tgather_strided_views_equal_torch_cat(o, case)
     else:
         raise ValueError(kind)
 
 
 def test_unmutated_copy_passes_every_pin_used_here(tmp_path):
     o = _compile(tmp_path, "identity", "int oracle_tgather(", "int oracle_tgather(")
-    for kind in ("tg_scheme", "tg_cat", "bf16", "int_exact", "f64", "chunked", "rows"):
+    for kind in ("tg_scheme", "tg_cat", "bf16", "int_exact", "f64", "chunked", "rows", "tg_strided"):
         _run_pin(kind, o)
 
 

@@ -291,3 +291,44 @@ def test_rows_variant_matches_full(oracle_mod):
     C, _ = oracle_mod.ag_matmul(shards, Bb)
     rows = np.array([0, 5, 23, 24, 47, 48, 71])
     assert np.array_equal(oracle_mod.ag_matmul_rows(shards, Bb, rows), C[rows])
+
+
+# ----------------------------------------------------------------------------- strided TGATHER
+
+
+@pytest.mark.parametrize("nranks", [1, 3, 8])
+def test_tgather_strided_dense_equals_dense_form(oracle_mod, nranks):
+    """With dense strides the strided form is the dense formula."""
+    rng = np.random.default_rng(nranks)
+    srcs = [rng.integers(-2**31, 2**31, (2, 3, 1, 5, 7)).astype(np.int32) for _ in range(nranks)]
+    ref = oracle_mod.tgather(srcs)
+    out = np.zeros_like(ref)
+    oracle_mod.tgather_strided(out, srcs)
+    assert np.array_equal(out, ref)
+
+
+@pytest.mark.parametrize("case", ["slices", "transposed_w", "padded_dst"])
+def test_tgather_strided_views_equal_torch_cat(oracle_mod, case):
+    """[TG] §7.3: GlobalTensor views with strides; torch.cat of the same views along DIM_3."""
+    g = torch.Generator().manual_seed(len(case))
+    nranks, shape = 4, (2, 1, 3, 6, 10)
+    if case == "transposed_w":
+        bases = [torch.randint(-1000, 1000, (2, 1, 3, 10, 6), generator=g, dtype=torch.int32) for _ in range(nranks)]
+        srcs = [b.transpose(3, 4) for b in bases]        # inner stride != 1
+    else:
+        bases = [torch.randint(-1000, 1000, (3, 2, 4, 9, 17), generator=g, dtype=torch.int32) for _ in range(nranks)]
+        srcs = [b[1:3, :1, ::1][:, :, 1:4, 2:8, 3:13] for b in bases]   # offset slices, padded rows
+    assert tuple(srcs[0].shape) == shape
+    ref = torch.cat(srcs, dim=3)
+    if case == "padded_dst":
+        big = torch.full((2, 1, 3, nranks * 6 + 3, 15), -5, dtype=torch.int32)
+        dst = big[:, :, :, 1:1 + nranks * 6, 2:12]
+    else:
+        big = torch.full((2, 1, 3, nranks * 6, 10), -5, dtype=torch.int32)
+        dst = big
+    out = oracle_mod.tgather_strided(dst.numpy(), [s.numpy() for s in srcs])
+    assert np.array_equal(np.asarray(dst.numpy()), ref.numpy())
+    if case == "padded_dst":
+        mask = torch.ones_like(big, dtype=torch.bool)
+        mask[:, :, :, 1:1 + nranks * 6, 2:12] = False
+        assert torch.all(big[mask] == -5)  # everything outside the destination view untouched

@@ -7,5 +7,5 @@ include/tgc.h); this package only builds it (``_build``), binds it with ctypes
 from ._lib import (  # noqa: F401
     TGCError, lib, tgc_ag_matmul, tgc_ag_matmul_ex, tgc_ag_matmul_noalloc, tgc_ag_matmul_schedule,
     tgc_ag_matmul_workspace_bytes, tgc_gemm_tile_shape, tgc_last_cuda_error, tgc_status_string,
-    tgc_tgather, tgc_tgather_ex, tgc_version,
+    tgc_tgather, tgc_tgather_ex, tgc_tgather_strided, tgc_version,
 )

@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
     L.tgc_tgather.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _i64, _i64, _i64,
                               ctypes.c_int, _vp]
     L.tgc_tgather.restype = ctypes.c_int
+    L.tgc_tgather_strided.argtypes = [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_vp), ctypes.POINTER(_i64),
+                                      ctypes.c_int, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp]
+    L.tgc_tgather_strided.restype = ctypes.c_int
     L.tgc_tgather_ex.argtypes = [ctypes.POINTER(TgatherArgs)]
     L.tgc_tgather_ex.restype = ctypes.c_int
     L.tgc_ag_matmul.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i64, _vp]
@@ -170,6 +173,20 @@ def tgc_tgather(dst, srcs, stream=None, check: bool = True) -> int:
     rc = lib().tgc_tgather(_ptr(dst), _ptrs(srcs), len(srcs), D0, D1, D2, H, W,
                            DTYPES[srcs[0].dtype], _stream(stream))
     return _check(rc, "tgc_tgather") if check else rc
+
+
+def tgc_tgather_strided(dst, srcs, stream=None, check: bool = True) -> int:
+    """TGATHER on strided 5-D views: srcs share one shape and one stride; dst is a
+    (D0,D1,D2,>=N*H,W) view of any strides (rows r*H+i are written)."""
+    D0, D1, D2, H, W = srcs[0].shape
+    st = srcs[0].stride()
+    if any(tuple(x.shape) != tuple(srcs[0].shape) or x.stride() != st for x in srcs):
+        raise ValueError("all sources must share one shape and one stride")
+    ss = (_i64 * 5)(*st)
+    ds = (_i64 * 5)(*dst.stride())
+    rc = lib().tgc_tgather_strided(_ptr(dst), ds, _ptrs(srcs), ss, len(srcs), D0, D1, D2, H, W,
+                                   DTYPES[srcs[0].dtype], _stream(stream))
+    return _check(rc, "tgc_tgather_strided") if check else rc
 
 
 def tgc_tgather_ex(dst, srcs, dst_rows3: int = 0, progress=None, counters=None, chunk_rows: int = 0,

@@ -431,6 +431,26 @@ int tgc_tgather(void *dst, const void *const *srcs, int nranks, int64_t D0, int6
     return tgather_impl(a);
 }
 
+int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const *srcs, const int64_t *src_strides,
+                        int nranks, int64_t D0, int64_t D1, int64_t D2, int64_t H, int64_t W, tgc_dtype dtype,
+                        cudaStream_t stream) {
+    if (nranks <= 0 || nranks > TGC_MAX_RANKS) return TGC_ERR_INVALID_ARG;
+    if (D0 < 0 || D1 < 0 || D2 < 0 || H < 0 || W < 0) return TGC_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (es == 0) return TGC_ERR_DTYPE;
+    if (D0 * D1 * D2 * H == 0 || W == 0) return TGC_OK;  // empty: nothing written
+    if (dst == nullptr || srcs == nullptr || dst_strides == nullptr || src_strides == nullptr)
+        return TGC_ERR_INVALID_ARG;
+    for (int k = 0; k < 5; ++k)
+        if (dst_strides[k] < 0 || src_strides[k] < 0) return TGC_ERR_INVALID_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (srcs[r] == nullptr) return TGC_ERR_INVALID_ARG;
+    if (!aligned(dst, es)) return TGC_ERR_ALIGN;
+    for (int r = 0; r < nranks; ++r)
+        if (!aligned(srcs[r], es)) return TGC_ERR_ALIGN;
+    return launch_tgather_strided(srcs, dst, nranks, D0, D1, D2, H, W, es, src_strides, dst_strides, stream);
+}
+
 int tgc_tgather_ex(const tgc_tgather_args *args) {
     if (args == nullptr) return TGC_ERR_INVALID_ARG;
     return tgather_impl(*args);

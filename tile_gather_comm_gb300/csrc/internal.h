@@ -33,6 +33,9 @@ struct TGatherLaunch {
     uint32_t epoch;
 };
 int launch_tgather(const TGatherLaunch &L, cudaStream_t stream);
+int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64_t D0, int64_t D1, int64_t D2,
+                           int64_t H, int64_t W, int es, const int64_t *src_strides, const int64_t *dst_strides,
+                           cudaStream_t stream);
 
 // Launch one of the GEMM kernels; arguments already validated.
 struct GemmLaunch {

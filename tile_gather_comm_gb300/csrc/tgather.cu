@@ -219,6 +219,107 @@ __global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams
     }
 }
 
+// Strided views ("CANN PTO-ISA TGATHER 指令深度解析", §7.3 and §8.1: GlobalTensor
+// views with a shape and a stride, shared by every source).  Thread g of the
+// grid copies vector g of the flattened (row, vector) space; rows are ordered
+// (rank, d0, d1, d2, i), so consecutive threads touch consecutive vectors of
+// one row.  INNER = rows are contiguous in source and destination (VW-byte
+// vectors); otherwise every element is copied on its own with both inner strides.
+struct TGStridedParams {
+    const uint8_t *srcs[TGC_MAX_RANKS];
+    uint8_t *dst;
+    int nranks;
+    int64_t D0, D1, D2, H;
+    int64_t ss[5], ds[5];  // byte strides
+    int64_t rows;          // nranks * D0 * D1 * D2 * H
+    int64_t nv;            // vectors (INNER) or elements per row
+};
+
+template <int VW, bool INNER>
+__global__ void __launch_bounds__(256) tgather_strided_kernel(const TGStridedParams p) {
+    using V = typename VecT<VW>::T;
+    const int64_t total = p.rows * p.nv;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = g / p.nv, v = g - row * p.nv;
+        int64_t t = row / p.H;
+        const int64_t i = row - t * p.H;
+        const int64_t d2 = t % p.D2;
+        t /= p.D2;
+        const int64_t d1 = t % p.D1;
+        t /= p.D1;
+        const int64_t d0 = t % p.D0;
+        const int r = (int)(t / p.D0);
+        const uint8_t *s = p.srcs[r] + d0 * p.ss[0] + d1 * p.ss[1] + d2 * p.ss[2] + i * p.ss[3];
+        uint8_t *d = p.dst + d0 * p.ds[0] + d1 * p.ds[1] + d2 * p.ds[2] + ((int64_t)r * p.H + i) * p.ds[3];
+        if (INNER) {
+            *reinterpret_cast<V *>(d + v * VW) = ld_stream(reinterpret_cast<const V *>(s + v * VW));
+        } else {
+            *reinterpret_cast<V *>(d + v * p.ds[4]) = *reinterpret_cast<const V *>(s + v * p.ss[4]);
+        }
+    }
+}
+
+int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64_t D0, int64_t D1, int64_t D2,
+                           int64_t H, int64_t W, int es, const int64_t *src_strides, const int64_t *dst_strides,
+                           cudaStream_t stream) {
+    TGStridedParams p{};
+    for (int r = 0; r < nranks; ++r) p.srcs[r] = static_cast<const uint8_t *>(srcs[r]);
+    p.dst = static_cast<uint8_t *>(dst);
+    p.nranks = nranks;
+    p.D0 = D0;
+    p.D1 = D1;
+    p.D2 = D2;
+    p.H = H;
+    for (int k = 0; k < 5; ++k) {
+        p.ss[k] = src_strides[k] * es;
+        p.ds[k] = dst_strides[k] * es;
+    }
+    p.rows = (int64_t)nranks * D0 * D1 * D2 * H;
+    const bool inner = p.ss[4] == es && p.ds[4] == es;
+    int vw = es;
+    if (inner) {
+        // widest vector every row start (source and destination) and the row length allow
+        uint64_t g = 16;
+        auto fold = [&](uint64_t x) { while (g > (uint64_t)es && (x % g) != 0) g >>= 1; };
+        for (int r = 0; r < nranks; ++r) fold(reinterpret_cast<uintptr_t>(srcs[r]));
+        fold(reinterpret_cast<uintptr_t>(dst));
+        const int64_t ext[4] = {D0, D1, D2, H};
+        for (int k = 0; k < 4; ++k)
+            if (ext[k] > 1) { fold((uint64_t)p.ss[k]); fold((uint64_t)p.ds[k]); }
+        if ((int64_t)nranks * H > 1) fold((uint64_t)p.ds[3]);
+        fold((uint64_t)(W * es));
+        vw = (int)g;
+    }
+    p.nv = inner ? W * es / vw : W;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t total = p.rows * p.nv;
+    int64_t grid = (total + 255) / 256;
+    const int64_t cap = (int64_t)sm_count(dev) * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const dim3 gd((unsigned)grid), bd(256);
+    if (inner) {
+        switch (vw) {
+            case 16: tgather_strided_kernel<16, true><<<gd, bd, 0, stream>>>(p); break;
+            case 8: tgather_strided_kernel<8, true><<<gd, bd, 0, stream>>>(p); break;
+            case 4: tgather_strided_kernel<4, true><<<gd, bd, 0, stream>>>(p); break;
+            case 2: tgather_strided_kernel<2, true><<<gd, bd, 0, stream>>>(p); break;
+            default: tgather_strided_kernel<1, true><<<gd, bd, 0, stream>>>(p); break;
+        }
+    } else {
+        switch (es) {
+            case 8: tgather_strided_kernel<8, false><<<gd, bd, 0, stream>>>(p); break;
+            case 4: tgather_strided_kernel<4, false><<<gd, bd, 0, stream>>>(p); break;
+            case 2: tgather_strided_kernel<2, false><<<gd, bd, 0, stream>>>(p); break;
+            default: tgather_strided_kernel<1, false><<<gd, bd, 0, stream>>>(p); break;
+        }
+    }
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+}
+
 static int pick_vw(const TGatherLaunch &L) {
     // Largest power of two <= 16 dividing every (src - dst) address difference;
     // then source and destination share their alignment modulo VW everywhere.
