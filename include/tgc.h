@@ -217,6 +217,15 @@ typedef enum tgc_pivot {
     TGC_PIVOT_READY_QUEUE = 3
 } tgc_pivot;
 
+/* Element type of C.  F8E4M3: float8 e4m3 ("fn": bias 7, no infinities,
+ * largest finite 448), round to nearest even and saturating at +-448 ([AGM]
+ * section MatMul 按需等待远端分片: the kernel's FP8_OUTPUT argument writes C
+ * as float8_e4m3fn).  Needs N % 16 == 0. */
+typedef enum tgc_out_format {
+    TGC_OUT_BF16 = 0,
+    TGC_OUT_F8E4M3 = 1
+} tgc_out_format;
+
 /*
  * Extended AllGather-MatMul.  Fields beyond tgc_ag_matmul's:
  *   a_out        device (M, K) bf16: the gathered A.  FUSED and UNFUSED write
@@ -255,6 +264,7 @@ typedef enum tgc_pivot {
  *                NULL the status word lives in the workspace (FUSED) or is
  *                not kept (UNFUSED / MM_ONLY without workspace).
  *   sync         nonzero: synchronize `stream` and return the device status.
+ *   out_format   element type of C (tgc_out_format; 0 = bf16).
  *   trace        optional device uint64 array of grid*TGC_TRACE_WORDS words
  *                (grid = the persistent CTA count actually launched, at most
  *                the SM count): per CTA, %globaltimer stamps and signal-wait
@@ -288,6 +298,7 @@ typedef struct tgc_ag_matmul_args {
     int sync;
     cudaStream_t stream;
     uint64_t *trace;
+    tgc_out_format out_format;
 } tgc_ag_matmul_args;
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);

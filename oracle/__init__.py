@@ -35,7 +35,7 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-shared", "-fPIC", "-std=c11", "-Wall", "-o", tmp, _SRC]
+           "-shared", "-fPIC", "-std=c11", "-Wall", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -55,6 +55,10 @@ def _bind(lib):
     lib.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
     lib.oracle_f32_to_bf16_array.argtypes = [vp, vp, i64]
     lib.oracle_f32_to_bf16_array.restype = None
+    lib.oracle_f32_to_e4m3_array.argtypes = [vp, vp, i64]
+    lib.oracle_f32_to_e4m3_array.restype = None
+    lib.oracle_ag_matmul_rows_e4m3.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp, i64, i64, i64, vp, i64, vp]
+    lib.oracle_ag_matmul_rows_e4m3.restype = ctypes.c_int
     lib.oracle_ag_matmul.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp, vp, vp, i64, i64, i64]
     lib.oracle_ag_matmul.restype = ctypes.c_int
     lib.oracle_ag_matmul_rows.argtypes = [ctypes.POINTER(vp), ctypes.c_int, vp, i64, i64, i64,
@@ -157,6 +161,32 @@ class Oracle:
         self._L.oracle_f32_to_bf16_array(_ptr(x), _ptr(y), x.size)
         return y
 
+    def f32_to_e4m3(self, x: np.ndarray) -> np.ndarray:
+        """float32 -> float8 e4m3 (fn) bit patterns (uint8), RNE, saturating at +-448."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.uint8)
+        self._L.oracle_f32_to_e4m3_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    @staticmethod
+    def e4m3_to_f64(bits):
+        return e4m3_to_f64(bits)
+
+    def ag_matmul_rows_e4m3(self, a_shards, B: np.ndarray, rows) -> np.ndarray:
+        """Sampled rows of C written as float8 e4m3 bit patterns (uint8)."""
+        shards = [np.ascontiguousarray(s, dtype=np.uint16) for s in a_shards]
+        R = len(shards)
+        Hs, K = shards[0].shape
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        N = B.shape[0]
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.zeros((rows.size, N), dtype=np.uint8)
+        rc = self._L.oracle_ag_matmul_rows_e4m3(_ptr_array(shards), R, _ptr(B), R * Hs, K, N,
+                                                _ptr(rows), rows.size, _ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle_ag_matmul_rows_e4m3 rejected the arguments (rc={rc})")
+        return out
+
     def f32_to_bf16_scalar(self, x: float) -> int:
         return int(self._L.oracle_f32_to_bf16_rne(ctypes.c_float(x)))
 
@@ -257,6 +287,25 @@ def f32_to_bf16(x):
 
 def f32_to_bf16_scalar(x):
     return _oracle().f32_to_bf16_scalar(x)
+
+
+def f32_to_e4m3(x):
+    return _oracle().f32_to_e4m3(x)
+
+
+def ag_matmul_rows_e4m3(a_shards, B, rows):
+    return _oracle().ag_matmul_rows_e4m3(a_shards, B, rows)
+
+
+def e4m3_to_f64(bits):
+    """Decode float8 e4m3 (fn) bit patterns to float64 (exact; NaN for S.1111.111)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0**-6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
 
 
 def ag_matmul(a_shards, B):

@@ -20,6 +20,7 @@
  * Parity status: every function below is pinned by tests/test_oracle_pins.py
  * (closed forms, library special cases, integer-exact cases, brute force).
  */
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -148,6 +149,58 @@ void oracle_f32_to_bf16_array(const float *x, uint16_t *y, int64_t n)
         y[i] = oracle_f32_to_bf16_rne(x[i]);
 }
 
+/*
+ * float32 -> float8 e4m3 ("fn" variant: 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN, so the largest finite
+ * magnitude is 1.110b * 2^8 = 448), round to nearest even, saturating: every
+ * finite or infinite input of magnitude >= 448 becomes +-448.  [AGM] section
+ * MatMul 按需等待远端分片: the kernel takes FP8_OUTPUT and writes C as
+ * float8_e4m3fn; the saturating conversion is the reading taken here.  Written
+ * from the format definition: subnormals are k * 2^-9 (k = 0..7), normals
+ * (1 + m/8) * 2^e with e in [-6, 8].  NaN -> 0x7F with the sign kept.
+ */
+uint8_t oracle_f32_to_e4m3_sat(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+        return (uint8_t)(sign | 0x7Fu);
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7Eu);
+    if (a < ldexp(1.0, -6)) {                 /* subnormal range: multiples of 2^-9 */
+        double q = a * 512.0;                  /* exact: a is a float, 512 a power of 2 */
+        double k = floor(q);
+        double rem = q - k;
+        if (rem > 0.5 || (rem == 0.5 && fmod(k, 2.0) != 0.0))
+            k += 1.0;
+        /* k == 8 is the smallest normal 2^-6, whose encoding is 0x08 as well */
+        return (uint8_t)(sign | (uint8_t)k);
+    }
+    int e;
+    double m = frexp(a, &e);                   /* a = m * 2^e, m in [0.5, 1) */
+    e -= 1;                                     /* a = (2m) * 2^e, 2m in [1, 2) */
+    double frac = (2.0 * m - 1.0) * 8.0;       /* mantissa in units of 1/8, exact */
+    double k = floor(frac);
+    double rem = frac - k;
+    if (rem > 0.5 || (rem == 0.5 && fmod(k, 2.0) != 0.0))
+        k += 1.0;
+    if (k == 8.0) {
+        k = 0.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && k > 6.0))
+        return (uint8_t)(sign | 0x7Eu);        /* rounded past 448: saturate */
+    return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | (int)k));
+}
+
+void oracle_f32_to_e4m3_array(const float *x, uint8_t *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = oracle_f32_to_e4m3_sat(x[i]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* AllGather then MatMul                                                     */
 /* ------------------------------------------------------------------------ */
@@ -220,6 +273,36 @@ int oracle_ag_matmul_rows(const uint16_t *const *a_shards, int R, const uint16_t
         const uint16_t *arow = a_shards[m / H] + (m % H) * K;
         for (int64_t n = 0; n < N; ++n)
             C_rows[t * N + n] = dot_row(arow, B + n * K, K);
+    }
+    return 0;
+}
+
+/*
+ * The same sampled rows with C written as float8 e4m3 (the FP8_OUTPUT variant
+ * of [AGM]'s kernel): identical fp32 sums, converted by oracle_f32_to_e4m3_sat.
+ */
+int oracle_ag_matmul_rows_e4m3(const uint16_t *const *a_shards, int R, const uint16_t *B,
+                               int64_t M, int64_t K, int64_t N,
+                               const int64_t *rows, int64_t nrows, uint8_t *C_rows)
+{
+    if (R <= 0 || M % R != 0)
+        return -1;
+    int64_t H = M / R;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= M)
+            return -1;
+    int64_t t;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (t = 0; t < nrows; ++t) {
+        int64_t m = rows[t];
+        const uint16_t *arow = a_shards[m / H] + (m % H) * K;
+        for (int64_t n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            const uint16_t *brow = B + n * K;
+            for (int64_t k = 0; k < K; ++k)
+                acc += oracle_bf16_to_f32(arow[k]) * oracle_bf16_to_f32(brow[k]);
+            C_rows[t * N + n] = oracle_f32_to_e4m3_sat(acc);
+        }
     }
     return 0;
 }

@@ -129,6 +129,8 @@ def test_ag_matmul_invalid_arguments():
     oob = (ctypes.c_int32 * 2)(0, 8)
     assert _ag(order=oob, n_order=2) == E.TGC_ERR_INVALID_ARG
     assert _lib.lib().tgc_ag_matmul_ex(None) == E.TGC_ERR_INVALID_ARG
+    assert _ag(out_format=1, N=72) == E.TGC_ERR_ALIGN       # fp8 C needs N % 16 == 0
+    assert _ag(out_format=5) == E.TGC_ERR_INVALID_ARG
 
 
 def test_ag_matmul_empty_problem_is_ok():

@@ -274,3 +274,64 @@ def test_trace_records_every_cta():
     assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
     assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
     assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])
+
+
+# ----------------------------------------------------------------------------- float8 e4m3 output
+
+
+def _e4m3_ulp(v):
+    """Spacing of e4m3 values at |v| (subnormal spacing 2^-9 below 2^-6)."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.maximum(a, 2.0**-6)))
+    return np.exp2(e - 3)
+
+
+def _run_fp8(run, **kw):
+    C8 = torch.zeros(run.cfg.M, run.cfg.N, dtype=torch.uint8, device=DEV)
+    run.epoch += 1
+    tgc.tgc_ag_matmul_ex(run.shards, run.B, C8, run.a, run.cfg.cb, progress=run.progress, epoch=run.epoch,
+                         workspace=run.ws, sync=True, out_format="f8e4m3", **kw)
+    return C8
+
+
+def test_fp8_output_integer_exact():
+    """Values in {-1, 0, 1}, K = 16: |C| <= 16, and integers up to 16 are exact in e4m3."""
+    g = torch.Generator().manual_seed(31)
+    R, H, K, N = 4, 64, 16, 272
+    si = [torch.randint(-1, 2, (H, K), generator=g) for _ in range(R)]
+    Bi = torch.randint(-1, 2, (N, K), generator=g)
+    cfg = AGConfig("int8out", R=R, H=H, K=K, N=N, cb=32, b_sigma=1.0)
+    run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bi.to(torch.bfloat16))
+    ref = (torch.cat(si) @ Bi.T).numpy().astype(np.float64)
+    for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue")):
+        C8 = _run_fp8(run, mode=mode, pivot=pivot)
+        assert np.array_equal(oracle.e4m3_to_f64(C8.cpu().numpy()), ref), mode
+
+
+def test_fp8_output_square_workload_within_one_step():
+    """Sampled rows against the oracle's fp8 rows: the fp32 sums differ only by summation
+    order, so the e4m3 results may differ by one step where a sum lies at a rounding boundary."""
+    cfg, shards, B = _inputs("square")
+    run = Run(cfg, shards, B)
+    C8 = _run_fp8(run)
+    rows = sample_rows(cfg, seed=0, per_block_random=1)
+    ref = oracle.e4m3_to_f64(oracle.ag_matmul_rows_e4m3([bits16(s) for s in shards], bits16(B), rows))
+    got = oracle.e4m3_to_f64(C8[rows].cpu().numpy())
+    diff = np.abs(got - ref)
+    assert np.all(diff <= _e4m3_ulp(ref) + 1e-12)
+    assert (diff > 0).mean() < 0.01
+    C8u = _run_fp8(run, mode="unfused")
+    assert torch.equal(C8, C8u), "fused and unfused fp8 outputs differ"
+
+
+def test_fp8_output_saturates():
+    """Sums beyond 448 saturate to +-448 (0x7E / 0xFE) instead of becoming NaN."""
+    g = torch.Generator().manual_seed(32)
+    R, H, K, N = 2, 128, 64, 256
+    si = [torch.ones(H, K) * 4 for _ in range(R)]
+    Bm = torch.ones(N, K) * 4
+    Bm[: N // 2] *= -1
+    cfg = AGConfig("sat", R=R, H=H, K=K, N=N, cb=64, b_sigma=1.0)
+    run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bm.to(torch.bfloat16))
+    C8 = _run_fp8(run).cpu().numpy()   # every sum is +-1024
+    assert np.all(C8[:, : N // 2] == 0xFE) and np.all(C8[:, N // 2:] == 0x7E)

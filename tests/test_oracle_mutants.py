@@ -35,6 +35,9 @@ MUTANTS = [
      "int64_t row0 = src_rank * H + (S - 1 - split_id) * cb;", ["chunked"]),
     ("strided_row_index", "int64_t row = (int64_t)r * H + i;", "int64_t row = (int64_t)r * H + (H - 1 - i);",
      ["tg_strided"]),
+    ("e4m3_truncate", "        k += 1.0;\n    if (k == 8.0) {", "        k += 0.0;\n    if (k == 8.0) {", ["e4m3"]),
+    ("e4m3_no_saturation", "if (a >= 448.0)\n        return (uint8_t)(sign | 0x7Eu);",
+     "if (a >= 480.0)\n        return (uint8_t)(sign | 0x7Fu);", ["e4m3"]),
     ("rows_wrong_shard", "const uint16_t *arow = a_shards[m / H] + (m % H) * K;",
      "const uint16_t *arow = a_shards[(m / H + 1) % R] + (m % H) * K;", ["rows"]),
 ]
@@ -74,6 +77,9 @@ def _run_pin(kind, o):
         pins.test_chunked_equals_gather_then_matmul(o, 0)
     elif kind == "rows":
         pins.test_rows_variant_matches_full(o)
+    elif kind == "e4m3":
+        pins.test_e4m3_rne_matches_torch_inside_range(o)
+        pins.test_e4m3_grid_points_ties_and_saturation(o)
     elif kind == "tg_strided":
         for case in ("slices", "transposed_w", "padded_dst"):
             pins.test_tgather_strided_views_equal_torch_cat(o, case)
@@ -83,7 +89,7 @@ def _run_pin(kind, o):
 
 def test_unmutated_copy_passes_every_pin_used_here(tmp_path):
     o = _compile(tmp_path, "identity", "int oracle_tgather(", "int oracle_tgather(")
-    for kind in ("tg_scheme", "tg_cat", "bf16", "int_exact", "f64", "chunked", "rows", "tg_strided"):
+    for kind in ("tg_scheme", "tg_cat", "bf16", "int_exact", "f64", "chunked", "rows", "tg_strided", "e4m3"):
         _run_pin(kind, o)
 
 

@@ -332,3 +332,55 @@ def test_tgather_strided_views_equal_torch_cat(oracle_mod, case):
         mask = torch.ones_like(big, dtype=torch.bool)
         mask[:, :, :, 1:1 + nranks * 6, 2:12] = False
         assert torch.all(big[mask] == -5)  # everything outside the destination view untouched
+
+
+# ----------------------------------------------------------------------------- float8 e4m3 output
+
+
+def _torch_e4m3_bits(x32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(x32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_rne_matches_torch_inside_range(oracle_mod):
+    """Inside the finite range torch's float8_e4m3fn cast is round-to-nearest-even."""
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        rng.uniform(-448, 448, 400_000), rng.uniform(-1, 1, 200_000),
+        rng.uniform(-2**-5, 2**-5, 200_000),  # subnormals and the smallest normals
+        np.exp2(rng.uniform(-12, 8.8, 200_000)) * rng.choice([-1, 1], 200_000),
+    ]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    assert np.array_equal(oracle_mod.f32_to_e4m3(x), _torch_e4m3_bits(x))
+
+
+def test_e4m3_grid_points_ties_and_saturation(oracle_mod):
+    grid = oracle_mod.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    finite = ~np.isnan(grid)
+    codes = np.arange(256, dtype=np.uint8)[finite]
+    # every representable value converts to itself (0x80 is -0)
+    assert np.array_equal(oracle_mod.f32_to_e4m3(grid[finite].astype(np.float32)), codes)
+    # midpoints between neighbours round to the even code
+    pos = np.sort(np.unique(grid[finite & (grid >= 0)]))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    lo = oracle_mod.f32_to_e4m3(pos[:-1].astype(np.float32))
+    hi = oracle_mod.f32_to_e4m3(pos[1:].astype(np.float32))
+    got = oracle_mod.f32_to_e4m3(mids)
+    assert np.all(np.where(lo % 2 == 0, got == lo, got == hi))
+    # saturation: the largest finite magnitude is 448 = 0x7E; everything beyond clamps there
+    big = np.array([448, 449, 464, 465, 480, 1e6, np.inf], dtype=np.float32)
+    assert np.all(oracle_mod.f32_to_e4m3(big) == 0x7E)
+    assert np.all(oracle_mod.f32_to_e4m3(-big) == 0xFE)
+    assert oracle_mod.f32_to_e4m3(np.array([np.nan], np.float32))[0] & 0x7F == 0x7F
+
+
+def test_ag_matmul_e4m3_rows_integer_exact(oracle_mod):
+    """Values in {-1, 0, 1} with K = 16: |C| <= 16, and integers up to 16 are exact in e4m3."""
+    g = torch.Generator().manual_seed(21)
+    R, H, K, N = 4, 8, 16, 24
+    si = [torch.randint(-1, 2, (H, K), generator=g) for _ in range(R)]
+    Bi = torch.randint(-1, 2, (N, K), generator=g)
+    rows = np.arange(R * H)
+    got = oracle_mod.ag_matmul_rows_e4m3([_bf16_bits(s.to(torch.bfloat16)) for s in si],
+                                         _bf16_bits(Bi.to(torch.bfloat16)), rows)
+    ref = (torch.cat(si) @ Bi.T).numpy().astype(np.float64)
+    assert np.array_equal(oracle_mod.e4m3_to_f64(got), ref)

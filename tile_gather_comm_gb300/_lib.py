@@ -28,6 +28,7 @@ NOALLOC_MAX_BLOCKS = 2048
 
 MODES = {"fused": 0, "unfused": 1, "mm_only": 2, "fused_ce": 3}
 PIVOTS = {"page": 0, "shard": 1, "none": 2, "ready_queue": 3}
+OUT_FORMATS = {"bf16": 0, "f8e4m3": 1}
 DTYPES = {
     torch.uint8: 0, torch.int8: 1, torch.float16: 2, torch.bfloat16: 3,
     torch.int32: 4, torch.float32: 5, torch.int64: 6, torch.float64: 7,
@@ -62,7 +63,7 @@ class AgMatmulArgs(ctypes.Structure):
         ("delay_ns", ctypes.POINTER(ctypes.c_uint32)),
         ("spin_timeout_ns", ctypes.c_uint64), ("group_m", ctypes.c_int), ("grid", ctypes.c_int),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("d_status", _vp),
-        ("sync", ctypes.c_int), ("stream", _vp), ("trace", _vp),
+        ("sync", ctypes.c_int), ("stream", _vp), ("trace", _vp), ("out_format", ctypes.c_int),
     ]
 
 
@@ -230,7 +231,7 @@ def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | No
                      mode: str = "fused", pivot: str = "page", progress=None, epoch: int = 1, order=None,
                      delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, grid: int = 0,
                      workspace=None, d_status=None, sync: bool = False, stream=None, trace=None,
-                     check: bool = True) -> int:
+                     out_format: str = "bf16", check: bool = True) -> int:
     """Extended AllGather-MatMul (see tgc.h).  ``order`` / ``delay_ns`` are host sequences."""
     R = len(a_shards) if a_shards is not None else 1
     K = B.shape[1]
@@ -253,7 +254,8 @@ def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | No
         progress=_ptr(progress), epoch=epoch, order=order_arr, n_order=n_order, delay_ns=delay_arr,
         spin_timeout_ns=spin_timeout_ns, group_m=group_m, grid=grid, workspace=_ptr(workspace),
         workspace_bytes=(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
-        d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream), trace=_ptr(trace))
+        d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream), trace=_ptr(trace),
+        out_format=OUT_FORMATS[out_format])
     rc = lib().tgc_ag_matmul_ex(ctypes.byref(a))
     return _check(rc, "tgc_ag_matmul_ex") if check else rc
 

@@ -166,7 +166,9 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     out.nblocks = flagged ? a.M / a.comm_block_rows : 0;
     if (a.M == 0 || a.N == 0) return 1;  // nothing to do
     if (a.K == 0) return TGC_ERR_INVALID_ARG;
+    if (a.out_format != TGC_OUT_BF16 && a.out_format != TGC_OUT_F8E4M3) return TGC_ERR_INVALID_ARG;
     if (a.K % 8 != 0 || a.N % 8 != 0) return TGC_ERR_ALIGN;
+    if (a.out_format == TGC_OUT_F8E4M3 && a.N % 16 != 0) return TGC_ERR_ALIGN;
     if (a.B == nullptr || a.C == nullptr || a.a_out == nullptr) return TGC_ERR_INVALID_ARG;
     if (!aligned(a.B, 16) || !aligned(a.C, 16) || !aligned(a.a_out, 16)) return TGC_ERR_ALIGN;
     if (a.mode != TGC_MODE_MM_ONLY) {
@@ -338,6 +340,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.timeout_ns = timeout;
     G.status = status;
     G.trace = a.trace;
+    G.out_fp8 = a.out_format == TGC_OUT_F8E4M3 ? 1 : 0;
     if (a.mode != TGC_MODE_MM_ONLY)
         for (int r = 0; r < a.nranks; ++r) G.shards[r] = a.a_shards[r];
 

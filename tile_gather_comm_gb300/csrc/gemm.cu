@@ -111,6 +111,7 @@ struct GemmParams {
     int num_kb;
     TileSchedule sched;
     uint16_t *C;
+    int out_fp8;  // C as float8 e4m3 (N bytes per row) instead of bf16
     int *status;
     uint64_t timeout_ns;       // flag waits
     uint64_t mbar_timeout_ns;  // pipeline waits
@@ -441,6 +442,27 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
             uint32_t v[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
             tmem_wait_ld();
+            if (p.out_fp8) {
+                // 32 columns -> 32 bytes: two 16-byte stores (N % 16 == 0)
+                if (m < p.M) {
+                    uint8_t *crow8 = reinterpret_cast<uint8_t *>(p.C) + (int64_t)m * p.N;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int n = n0 + j * 32 + c * 16;
+                        if (n < p.N) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const int b = c * 16 + q4 * 4;
+                                w[q4] = (uint32_t)pack_e4m3x2(v[b + 0], v[b + 1]) |
+                                        ((uint32_t)pack_e4m3x2(v[b + 2], v[b + 3]) << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(crow8 + n) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                continue;
+            }
             if (m < p.M) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -829,6 +851,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     const int64_t rows_per_rank = L.M / L.nranks;
     p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, C::kTileM, p.sched.num_pid_m);
     p.C = static_cast<uint16_t *>(L.C);
+    p.out_fp8 = L.out_fp8;
     p.status = L.status;
     p.timeout_ns = L.timeout_ns;
     p.mbar_timeout_ns = 4 * L.timeout_ns + 100ull * 1000 * 1000;

@@ -64,6 +64,7 @@ struct GemmLaunch {
     uint64_t *ws_ring;      // tile rows (READY_QUEUE)
     int32_t *status;
     uint64_t *trace;        // optional, kTraceWords per CTA
+    int out_fp8;            // C as float8 e4m3 (saturating) instead of bf16
 };
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 

@@ -389,6 +389,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
     return r;
 }
 
+// Two fp32 -> packed float8 e4m3 (round to nearest even, saturating at the
+// largest finite magnitude); `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(uint32_t lo_bits, uint32_t hi_bits) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
+    return r;
+}
+
 // ---------------------------------------------------------------- UMMA descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile
