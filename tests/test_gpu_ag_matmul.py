@@ -337,3 +337,34 @@ def test_fp8_output_saturates():
     run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bm.to(torch.bfloat16))
     C8 = _run_fp8(run).cpu().numpy()   # every sum is +-1024
     assert np.all(C8[:, : N // 2] == 0xFE) and np.all(C8[:, N // 2:] == 0x7E)
+
+
+# ----------------------------------------------------------------------------- stress
+
+
+def test_stress_random_orders_delays_pivots_bit_exact():
+    """Many calls with random release orders, delays, tile orders, ranks and grid sizes on
+    one workspace: every result bit-identical to the unfused path, `a` refilled with NaN
+    before each call so that a tile reading a block before its flag would show up in C."""
+    cfg, shards, B = _custom(4, 512, 256, 768, 64, seed=77)
+    run = Run(cfg, shards, B)
+    run(mode="unfused")
+    ref = run.C.clone()
+    g = torch.Generator().manual_seed(78)
+    pivots = ["page", "shard", "none", "ready_queue"]
+    for i in range(150):
+        order = torch.randperm(cfg.nblocks, generator=g).tolist()
+        delay = torch.randint(0, 5000, (cfg.nblocks,), generator=g).tolist() if i % 3 == 0 else None
+        pivot = pivots[int(torch.randint(0, 4, (1,), generator=g))]
+        rank = int(torch.randint(0, cfg.R, (1,), generator=g))
+        grid = [0, 2, 8, 40][int(torch.randint(0, 4, (1,), generator=g))]
+        run.a.view(torch.int16).fill_(-1)
+        run.C.zero_()
+        run(order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid)
+        assert torch.equal(run.C, ref), (i, pivot, rank, grid)
+        assert torch.equal(run.a, torch.cat(run.shards)), i
+    # status word, ticket dispenser and per-block counters are zero again (the workspace also
+    # keeps the device copies of the last order / delay arrays, which need no clearing)
+    ws = run.ws.cpu()
+    assert torch.all(ws[:4] == 0) and torch.all(ws[64:80] == 0)
+    assert torch.all(ws[128:128 + 4 * cfg.nblocks] == 0)
