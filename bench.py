@@ -317,9 +317,14 @@ def run_ours(args, dist: Dist):
     if not args.quick:
         # The comparison lines are timed interleaved (rounds of every variant, median per
         # variant), so that slow drifts of the power-capped clock do not bias their ratios.
+        a_full = torch.cat(shards)
+
+        def cublas():  # context only: the vendor library GEMM on the gathered A, same shapes
+            torch.matmul(a_full, B.T, out=C)
         variants = {"fused": lambda: call("fused"), "unfused": lambda: call("unfused"),
                     "mm_only": lambda: call("mm_only"),
-                    "ready_queue": lambda: call("fused", pivot="ready_queue")}
+                    "ready_queue": lambda: call("fused", pivot="ready_queue"),
+                    "cublas_gemm": cublas}
         if cfg.skewed:
             variants["no_delay"] = lambda: call("fused", delays=False)
         med = time_interleaved(variants, args.steps, dist, stream)
@@ -330,6 +335,9 @@ def run_ours(args, dist: Dist):
         res["unfused"]["kernels_per_step"] = 2
         res["mm_only"]["frac_of_peak"] = round(flops / (med["mm_only"] * 1e-3) * 1e-12 / peaks["bf16_tflops"], 4)
         res["ready_queue"]["note"] = "same workload, READY_QUEUE tile order"
+        res["cublas_gemm"]["note"] = ("context: torch.matmul (cuBLAS) on the already gathered A, "
+                                      "same shapes; not part of this library")
+        del a_full
         res["fused_over_unfused"] = round(med["unfused"] / med["fused"], 4)
         res["comparison_timing"] = "interleaved rounds (6), median per variant"
         res["tgather"] = bench_tgather(TG_CONFIGS["bw_f16"], dev, stream, dist, peaks, peaks_kind, args)
