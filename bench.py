@@ -214,23 +214,36 @@ def time_interleaved(variants: dict, steps: int, dist: Dist, stream, rounds: int
     return {n: statistics.median(v) for n, v in times.items()}
 
 
-def time_device(fn, steps: int, warmup: int, dist: Dist, stream):
-    """Barrier + sync, then CUDA events on `stream` around exactly `steps` calls."""
+def time_device(fn, steps: int, warmup: int, dist: Dist, stream, per_step: list | None = None):
+    """Barrier + sync, then CUDA events on `stream` around exactly `steps` calls.
+    If `per_step` is a list, an event is also recorded after every call and the
+    per-call times (ms) are appended to it."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step is not None else 2)]
+    ev[0].record(stream)
+    for i in range(steps):
         fn()
-    e1.record(stream)
+        if per_step is not None:
+            ev[i + 1].record(stream)
+    ev[-1].record(stream)
     torch.cuda.synchronize()
     dist.barrier()
-    return e0.elapsed_time(e1) / steps
+    if per_step is not None:
+        per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    return ev[0].elapsed_time(ev[-1]) / steps
+
+
+def percentiles(xs: list, qs=(10, 50, 90)) -> dict:
+    """Nearest-rank percentiles of a list of numbers."""
+    v = sorted(xs)
+    if not v:
+        return {}
+    return {f"p{q}": round(v[min(len(v) - 1, max(0, -(-q * len(v) // 100) - 1))], 4) for q in qs}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -289,7 +302,8 @@ def run_ours(args, dist: Dist):
     sampler.start()
 
     launches[0] = 0
-    ms_fused = time_device(lambda: call("fused"), args.steps, args.warmup, dist, stream)
+    step_ms = []
+    ms_fused = time_device(lambda: call("fused"), args.steps, args.warmup, dist, stream, per_step=step_ms)
     fused_launches_timed = args.steps  # one kernel per fused call
     value, ms_max = aggregate(ms_fused, flops, dist)
     kernel_tflops = flops / (ms_fused * 1e-3) * 1e-12
@@ -307,6 +321,7 @@ def run_ours(args, dist: Dist):
             "timing": "CUDA events on the launching stream around exactly `steps` calls, max over ranks",
         },
         "gpu_launches": fused_launches_timed,
+        "step_ms_percentiles": percentiles(step_ms),
     }
     prof = profiled_traffic("ag_gemm_fused_large_skewed.md", KERNEL_SOURCES) if cfg.name == "large_skewed" else None
     res["roofline"] = {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peaks["bf16_tflops"],

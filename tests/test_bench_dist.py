@@ -65,3 +65,12 @@ def test_reference_arm_prints_on_rank0_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_percentiles_nearest_rank():
+    import bench
+    assert bench.percentiles(list(range(1, 11))) == {"p10": 1, "p50": 5, "p90": 9}
+    assert bench.percentiles([3.0]) == {"p10": 3.0, "p50": 3.0, "p90": 3.0}
+    assert bench.percentiles([]) == {}
+    # order of the input does not matter
+    assert bench.percentiles([9, 1, 5, 3, 7]) == bench.percentiles([1, 3, 5, 7, 9]) == {"p10": 1, "p50": 5, "p90": 9}

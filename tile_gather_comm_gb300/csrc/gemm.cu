@@ -24,16 +24,19 @@
 // single-CTA variant (128 x 256 tiles, cta_group::1) is kept behind the CG
 // template parameter.
 //
-// CTA anatomy (256 threads, one CTA per SM, persistent over tiles):
+// CTA anatomy (one CTA per SM, persistent over tiles; 256 threads, 384 for
+// the fused kernel with its extra copy warps):
 //   warp 0     scheduler + flag wait + TMA loads of this CTA's A (128x64) and
 //              B (128x64 per CTA of a pair, 256x64 alone) into a multi-stage
 //              shared-memory ring (128-byte swizzle)
 //   warp 1     TMEM owner; one lane (of the even CTA) issues tcgen05.mma into
 //              one of two TMEM accumulators (2 x 256 fp32 columns)
-//   warp 2     (FUSED) copy producer: bulk async copies global -> shared ->
-//              global of 8 KiB pieces of comm blocks, pieces handed out by a
-//              global ticket so any resident CTA can copy any block; the last
-//              piece of a block publishes its flag
+//   warps 2, 3, 8..11  (FUSED) copy producer: 64 KiB pieces of comm blocks,
+//              handed out by a global ticket so any resident CTA can copy any
+//              block, moved with 16-byte register loads and stores (or, with
+//              TGC_COPY_LSU=0, by warp 2 alone with bulk async copies through
+//              shared memory); the piece that completes a block publishes its
+//              flag
 //   warps 4..7 epilogue: tcgen05.ld of the accumulator (one TMEM lane quarter
 //              per warp), fp32 -> bf16 round-to-nearest-even, stores to C
 // The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
@@ -63,6 +66,21 @@ namespace tgc {
 #ifndef TGC_COPY_SLOTS
 #define TGC_COPY_SLOTS 4         // staging slots of the copy producer
 #endif
+// Copy producer: 0 = bulk async copies through shared-memory slots (the TMA
+// unit), 1 = 16-byte vector loads and stores through registers (the load/store
+// units) by warps 2 and 3.
+#ifndef TGC_COPY_LSU
+#define TGC_COPY_LSU 1
+#endif
+#ifndef TGC_COPY_VEC
+#define TGC_COPY_VEC 32          // vectors per lane in flight in the register copy
+#endif
+#ifndef TGC_COPY_WARPS
+#define TGC_COPY_WARPS 6         // register-copy warps: 2 and 3, then extra warps 8, 9, ...
+#endif
+#ifndef TGC_COPY_LEAD_WAVES
+#define TGC_COPY_LEAD_WAVES 2    // waves of local tiles up front that let the copy run on two warps
+#endif
 // L2 policies: 0 = default, 1 = evict_first, 2 = evict_last, 3 = evict_normal
 #ifndef TGC_COPY_HINT
 #define TGC_COPY_HINT 0          // producer's bulk loads of the shards and stores into `a`
@@ -78,7 +96,13 @@ __device__ __forceinline__ uint64_t make_policy(int kind) {
     return kind == 1 ? policy_evict_first() : kind == 2 ? policy_evict_last() : policy_evict_normal();
 }
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // warps 0..7: tile loads, MMA, copy (2, 3), epilogue (4..7)
+constexpr int kCopyWarps = TGC_COPY_LSU ? TGC_COPY_WARPS : 1;
+static_assert(kCopyWarps >= 1 && kCopyWarps <= 8, "copy warps");
+// Threads per CTA: the fused kernel with a register copy adds warps 8.. when
+// it runs more than two copy warps.
+template <bool FUSED, bool PROD>
+constexpr int kThreadsOf = (FUSED && PROD && TGC_COPY_LSU && kCopyWarps > 2) ? 32 * (6 + kCopyWarps) : kThreads;
 constexpr int kSlots = TGC_COPY_SLOTS;
 constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
 constexpr int kPieceBytes = 65536;      // unit of the ticket dispenser and of block completion
@@ -98,6 +122,10 @@ struct Cfg {
     static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
     static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
 };
+
+// Only the bulk copy producer stages through shared memory.
+template <bool FUSED, bool PROD>
+constexpr bool kUsesSlots = FUSED && PROD && !TGC_COPY_LSU;
 
 template <int CG, bool SLOTS>
 constexpr int smem_bytes() {
@@ -148,6 +176,7 @@ struct GemmParams {
     const uint32_t *delay_ns;  // device copy in the workspace, or null
     uint32_t *counters;
     uint32_t *tickets;   // [0] piece ticket, [1] finished producers, [2] ready-ring tail, [3] finished CTAs
+    int copy_warps;      // register copy: warps that take pieces (the others idle)
     uint64_t *trace;  // optional: kTraceWords per CTA
     // ready-queue order (FUSED only)
     int rq;               // nonzero: READY_QUEUE tile order
@@ -305,7 +334,7 @@ template <int CG, bool FUSED, bool PROD>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint64_t *helpbar, uint32_t crank, int lane) {
-    using C = Cfg<CG, FUSED && PROD>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     uint32_t it = 0;
     bool ok = true;
     uint64_t wait_ns = 0, waited_tiles = 0, load_stall_ns = 0;
@@ -413,7 +442,7 @@ template <int CG, bool FUSED, bool PROD>
 __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, uint32_t crank,
                          int lane) {
-    using C = Cfg<CG, FUSED && PROD>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
@@ -461,7 +490,7 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
 template <int CG, bool FUSED, bool PROD>
 __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
                               uint32_t crank, int warp, int lane) {
-    using C = Cfg<CG, FUSED && PROD>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     // the accumulator is released on the even CTA's barrier
@@ -722,20 +751,95 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
     }
 }
 
+constexpr int kCopyVec = TGC_COPY_VEC;
+
+// 16-byte load through the non-coherent path without L1 allocation: the shards
+// are read-only while the kernel runs and every byte is read once.
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+// The register copy producer (warps 2, 3 and 8.., TGC_COPY_LSU): each warp takes
+// pieces from the same ticket dispenser as the bulk producer and moves them
+// with coalesced 16-byte loads into registers and stores out of them,
+// kCopyVec vectors per lane in flight.  The tile loads keep the SM's TMA unit
+// busy; these copies bypass it.  After its stores every lane fences at gpu
+// scope (and for the async proxy that the consumers' tile loads use); lane 0
+// then retires the piece, and the piece that completes its block publishes it.
+__device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
+    __shared__ uint32_t s_pieces[kCopyWarps];
+    __shared__ uint64_t s_last[kCopyWarps];
+    const int cw = warp < 4 ? warp - 2 : warp - 6;  // index among the copy warps
+    const uint32_t total = (uint32_t)p.n_order * (uint32_t)p.pieces_per_block;
+    const uint64_t t_first = p.trace != nullptr ? globaltimer_ns() : 0;
+    uint32_t pieces = 0;
+    for (;;) {
+        if (cw >= p.copy_warps) break;
+        uint32_t tk = total;
+        if (lane == 0 && ld_status(p.status) == 0) tk = atom_add_relaxed_gpu(p.tickets, 1u);
+        tk = __shfl_sync(0xffffffffu, tk, 0);
+        if (tk >= total) break;
+        const Piece pc = piece_of(p, tk);
+        const uint4 *src = reinterpret_cast<const uint4 *>(pc.src);
+        uint4 *dst = reinterpret_cast<uint4 *>(pc.dst);
+        const int nvec = (int)(pc.bytes / 16u);  // block bytes are a multiple of 16 (K % 8 == 0)
+        for (int base = 0; base < nvec; base += 32 * kCopyVec) {
+            uint4 r[kCopyVec];
+#pragma unroll
+            for (int j = 0; j < kCopyVec; ++j) {
+                const int v = base + j * 32 + lane;
+                if (v < nvec) r[j] = ld_nc_v4(src + v);
+            }
+#pragma unroll
+            for (int j = 0; j < kCopyVec; ++j) {
+                const int v = base + j * 32 + lane;
+                if (v < nvec) dst[v] = r[j];
+            }
+        }
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) retire_piece(p, tk);
+        ++pieces;
+    }
+    if (p.trace != nullptr) {
+        if (lane == 0) {
+            s_pieces[cw] = pieces;
+            s_last[cw] = globaltimer_ns();
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kCopyWarps) : "memory");  // the copy warps only
+        if (cw == 0 && lane == 0) {
+            uint64_t last = 0;
+            uint32_t sum = 0;
+            for (int i = 0; i < kCopyWarps; ++i) {
+                last = s_last[i] > last ? s_last[i] : last;
+                sum += s_pieces[i];
+            }
+            p.trace[blockIdx.x * kTraceWords + kTrCopyFirst] = t_first;
+            p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = last;
+            p.trace[blockIdx.x * kTraceWords + kTrPieces] = sum;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int CG, bool FUSED, bool PROD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-    using C = Cfg<CG, FUSED && PROD>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kAStage;
     uint8_t *sSlot = sB + C::kStages * C::kBStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (FUSED && PROD ? kSlots * kSlotBytes : 0));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (kUsesSlots<FUSED, PROD> ? kSlots * kSlotBytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
@@ -775,9 +879,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         role_tma<CG, FUSED, PROD>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, helpbar, crank, lane);
     } else if (warp == 1) {
         role_mma<CG, FUSED, PROD>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
-    } else if (warp == 2) {
-        if (FUSED && PROD) role_copy(p, sSlot, slotbar, lane);
-    } else if (warp >= 4) {
+    } else if (warp == 2 || warp == 3 || warp >= 8) {
+        if (FUSED && PROD) {
+            if (TGC_COPY_LSU) {
+                if (warp < 4 ? warp - 2 < kCopyWarps : true) role_copy_lsu(p, warp, lane);
+            } else if (warp == 2) {
+                role_copy(p, sSlot, slotbar, lane);
+            }
+        }
+    } else {
         role_epilogue<CG, FUSED, PROD>(p, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
@@ -847,7 +957,7 @@ static int set_smem_attr() {
     static std::once_flag once;
     std::call_once(once, [] {
         err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes<CG, FUSED && PROD>());
+                                   smem_bytes<CG, kUsesSlots<FUSED, PROD>>());
     });
     return err == cudaSuccess ? TGC_OK : cuda_fail(err);
 }
@@ -866,8 +976,8 @@ static int max_clusters(int sms) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes<CG, FUSED && PROD>();
+        cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>>();
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
@@ -890,14 +1000,38 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CG, FUSED && PROD>();
+    cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD>, tmA, tmL, tmB, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
+}
+
+// Copy intensity of the register copy.  While the first TGC_COPY_LEAD_WAVES
+// waves of the tile order reach rows outside the caller's shard, tiles wait
+// for the copy, and every copy warp runs.  When the caller's own rows keep
+// every cluster busy for that long, two warps deliver the remote blocks in
+// time, and a faster copy would only compete with the GEMM's operand loads
+// for HBM.
+static int copy_warps_for(const GemmParams &p, int nclusters) {
+    using C = Cfg<kCG, false>;
+    const int horizon = TGC_COPY_LEAD_WAVES * nclusters;
+    bool urgent = false;
+    if (p.rq) {
+        urgent = p.rq_local_rows * p.sched.num_pid_n < horizon;
+    } else {
+        for (int t = 0; t < horizon && t < p.sched.num_tiles && !urgent; ++t) {
+            int pm = 0, pn = 0;
+            p.sched.tile(t, pm, pn);
+            const int m0 = pm * C::kTileM;
+            const int m1 = m0 + C::kTileM < p.M ? m0 + C::kTileM : p.M;
+            urgent = m0 < p.local_row0 || m1 > p.local_row1;
+        }
+    }
+    return urgent || kCopyWarps < 2 ? kCopyWarps : 2;
 }
 
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
@@ -983,6 +1117,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
     if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
     if (nclusters < 1) nclusters = 1;
+    if (variant == 1) p.copy_warps = copy_warps_for(p, nclusters);
     return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, p, nclusters, stream)
          : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, p, nclusters, stream)
                         : launch<kCG, true, false>(tmA, tmL, tmB, p, nclusters, stream);
