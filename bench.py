@@ -255,8 +255,8 @@ def run_ours(args, dist: Dist):
 
     import tile_gather_comm_gb300 as tgc
     from tile_gather_comm_gb300 import _build
-    from tile_gather_comm_gb300.workloads import (AG_CONFIGS, TG_CONFIGS, make_ag_inputs, make_release_schedule,
-                                                  make_tg_inputs)
+    from tile_gather_comm_gb300.workloads import (AG_CONFIGS, TG_CONFIGS, TGConfig, make_ag_inputs,
+                                                  make_release_schedule, make_tg_inputs)
 
     _build.build()
     tgc.lib()
@@ -358,6 +358,12 @@ def run_ours(args, dist: Dist):
         res["tgather"] = bench_tgather(TG_CONFIGS["bw_f16"], dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_ragged_i32"] = bench_tgather(TG_CONFIGS["ragged_i32"], dev, stream, dist, peaks,
                                                   peaks_kind, args)
+        # context: the same kernel on 8x taller sources, where the per-launch start and drain
+        # (about 2 us, fixed) weigh 8x less
+        long_cfg = TGConfig("bw_f16_long", 8, (2, 1, 1, 8192, 1024), torch.float16, "normal")
+        res["tgather_context_long"] = bench_tgather(long_cfg, dev, stream, dist, peaks, peaks_kind, args)
+        res["tgather_context_long"]["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the "
+                                               "TGATHER workload; per-launch start and drain amortised")
     res["clocks"] = sampler.stop()
 
     if not args.quick:
@@ -442,7 +448,7 @@ def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
     ms = ms_graph / nsets
     gbs, _ = aggregate(ms, per_set, dist, scale=1e-9)
     per_gpu = per_set / (ms * 1e-3) * 1e-9
-    src_name = "tgather_bw_f16.md" if tcfg.name == "bw_f16" else "tgather_ragged_i32.md"
+    src_name = {"bw_f16": "tgather_bw_f16.md", "ragged_i32": "tgather_ragged_i32.md"}.get(tcfg.name, "")
     out = {
         "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(ms * 1e3, 3),
         "config": f"{tcfg.nranks} x {str(tcfg.dtype).replace('torch.', '')} {tcfg.shape} -> dst DIM_3 x{tcfg.nranks}",

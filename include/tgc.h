@@ -319,6 +319,7 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 #define TGC_TRACE_LOAD_STALL_NS 11 /* TMA issuer: time waiting for free stages       */
 #define TGC_TRACE_HELP_PIECES 12 /* tile loader: pieces it copied while its first tile
                                     waited for remote data (start-up assist)         */
+#define TGC_TRACE_COPY_WARPS 13  /* producer: warps of this CTA that took pieces     */
 
 /*
  * tgc_ag_matmul_noalloc -- the fused AllGather-MatMul of tgc_ag_matmul with

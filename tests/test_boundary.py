@@ -210,3 +210,14 @@ def test_schedule_rejects_bad_arguments():
         tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 4, "page", 8, 1, 0)
     with pytest.raises(tgc.TGCError):
         tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 0, "page", 8, 2, 2)
+
+
+def test_trace_word_indices_match_header():
+    import re
+    from tile_gather_comm_gb300 import _lib
+    hdr = open(os.path.join(ROOT, "include", "tgc.h"), encoding="utf-8").read()
+    defs = {m.group(1).lower(): int(m.group(2)) for m in re.finditer(r"#define TGC_TRACE_([A-Z_]+)\s+(\d+)", hdr)}
+    words = defs.pop("words")
+    assert words == _lib.TRACE_WORDS
+    assert defs == _lib.TRACE
+    assert max(defs.values()) < words

@@ -278,6 +278,29 @@ def test_trace_records_every_cta():
     assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])
 
 
+def test_copy_intensity_follows_local_lead():
+    """The producer runs on two warps when the caller's own tiles fill the first two waves of the
+    tile order, and on every copy warp when the first waves reach remote rows; C is the same."""
+    seen = {}
+    for label, R, H in (("lead", 2, 4096), ("urgent", 8, 512)):
+        cfg, shards, B = _custom(R, H, 64, 4096, 256, seed=21)
+        run = Run(cfg, shards, B)
+        run(mode="unfused")
+        ref = run.C.clone()
+        trace = torch.zeros(152 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+        run.C.zero_()
+        run(trace=trace)
+        assert torch.equal(run.C, ref), label
+        t = trace.view(-1, _lib.TRACE_WORDS).cpu()
+        used = t[t[:, _lib.TRACE["start"]] > 0]
+        warps = set(int(w) for w in used[:, _lib.TRACE["copy_warps"]].tolist())
+        assert len(warps) == 1, (label, warps)
+        seen[label] = warps.pop()
+        assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
+    assert 1 <= seen["lead"] <= 2
+    assert seen["urgent"] >= seen["lead"]
+
+
 # ----------------------------------------------------------------------------- float8 e4m3 output
 
 

@@ -191,7 +191,7 @@ struct GemmParams {
 constexpr int kTraceWords = 16;
 enum : int {
     kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles,
-    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrHelpPieces
+    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrHelpPieces, kTrCopyWarps
 };
 
 // mbar_wait that adds the time it blocked to *acc (only when tracing).
@@ -748,6 +748,7 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
         p.trace[blockIdx.x * kTraceWords + kTrCopyFirst] = t_first;
         p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = globaltimer_ns();
         p.trace[blockIdx.x * kTraceWords + kTrPieces] = pieces;
+        p.trace[blockIdx.x * kTraceWords + kTrCopyWarps] = 1;
     }
 }
 
@@ -822,6 +823,7 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
             p.trace[blockIdx.x * kTraceWords + kTrCopyFirst] = t_first;
             p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = last;
             p.trace[blockIdx.x * kTraceWords + kTrPieces] = sum;
+            p.trace[blockIdx.x * kTraceWords + kTrCopyWarps] = (uint64_t)p.copy_warps;
         }
     }
 }
