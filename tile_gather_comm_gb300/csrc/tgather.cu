@@ -51,6 +51,10 @@ namespace tgc {
 #ifndef TGC_TG_CTAS_PER_SM
 #define TGC_TG_CTAS_PER_SM 8   // CTAs per SM in one wave
 #endif
+#ifndef TGC_TG_CHUNK
+#define TGC_TG_CHUNK 32768     // flat kernel: shares above this many bytes are cut into chunks
+                               // dealt round-robin over the CTAs (0: one contiguous share each)
+#endif
 
 constexpr int kTGThreads = TGC_TG_THREADS;
 constexpr int kTGUnroll = TGC_TG_UNROLL;
@@ -165,16 +169,19 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
 }
 
 // Flat variant (no progress release): the work space is the concatenation of
-// all (slab, rank) runs, and CTA c copies the c-th of gridDim.x equal,
-// 16-byte-aligned shares of it -- every CTA moves the same number of bytes,
-// so a grid of whole waves finishes together.  A share may span several runs;
-// each (run, share) intersection is copied with VW-byte vectors between
-// element-wise heads and tails.  The kernel is launched with programmatic
+// all (slab, rank) runs, cut into gridDim.x equal, 16-byte-aligned shares --
+// every CTA of the one full wave moves the same number of bytes, so they
+// finish together.  A share larger than TGC_TG_CHUNK is dealt as chunks
+// instead: CTA c copies chunks c, c + gridDim.x, ..., so at any moment the
+// grid works on one compact window of memory rather than on gridDim.x far-apart
+// streams (measured: 6.38 vs 6.02 TB/s on 537 MB, unchanged on 67 MB).  A
+// range may span several runs; each (run, range) intersection is copied with
+// VW-byte vectors between element-wise heads and tails.  The kernel is launched with programmatic
 // stream serialization: it lets the next launch in the stream be scheduled as
 // soon as every CTA has started, and waits for the previous grid's completion
 // (griddepcontrol.wait) before touching memory.
 template <int VW>
-__global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams p, int64_t share) {
+__global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams p, int64_t share, int64_t stride) {
     using V = typename VecT<VW>::T;
 #if TGC_TG_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -182,40 +189,44 @@ __global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams
 #endif
     const int tid = threadIdx.x;
     const int64_t total = p.nslab * p.nranks * p.run_bytes;
-    int64_t lo = (int64_t)blockIdx.x * share;
-    const int64_t hi = lo + share < total ? lo + share : total;
-    while (lo < hi) {
-        const int64_t run = lo / p.run_bytes;         // run = slab * nranks + r
-        const int64_t off = lo - run * p.run_bytes;   // offset inside the run
-        const int64_t end_in_run = (hi - run * p.run_bytes) < p.run_bytes ? (hi - run * p.run_bytes) : p.run_bytes;
-        const int64_t len = end_in_run - off;
-        const int64_t slab = run / p.nranks;
-        const int r = (int)(run - slab * p.nranks);
-        const uint8_t *src = p.srcs[r] + slab * p.run_bytes + off;
-        uint8_t *dst = p.dst + slab * p.dst_slab_bytes + (int64_t)r * p.run_bytes + off;
+    // ranges [first, first + share), then every `stride` bytes (stride 0: one range)
+    for (int64_t first = (int64_t)blockIdx.x * share; first < total; first += stride) {
+        int64_t lo = first;
+        const int64_t hi = lo + share < total ? lo + share : total;
+        while (lo < hi) {
+            const int64_t run = lo / p.run_bytes;         // run = slab * nranks + r
+            const int64_t off = lo - run * p.run_bytes;   // offset inside the run
+            const int64_t end_in_run = (hi - run * p.run_bytes) < p.run_bytes ? (hi - run * p.run_bytes) : p.run_bytes;
+            const int64_t len = end_in_run - off;
+            const int64_t slab = run / p.nranks;
+            const int r = (int)(run - slab * p.nranks);
+            const uint8_t *src = p.srcs[r] + slab * p.run_bytes + off;
+            uint8_t *dst = p.dst + slab * p.dst_slab_bytes + (int64_t)r * p.run_bytes + off;
 
-        int64_t head = (int64_t)((VW - (reinterpret_cast<uintptr_t>(src) % VW)) % VW);
-        if (head > len) head = len;
-        const int64_t nvec = (len - head) / VW;
-        const int64_t body_end = head + nvec * VW;
-        const V *vs = reinterpret_cast<const V *>(src + head);
-        V *vd = reinterpret_cast<V *>(dst + head);
-        for (int64_t base = 0; base < nvec; base += (int64_t)kTGThreads * kTGUnroll) {
-            V reg[kTGUnroll];
+            int64_t head = (int64_t)((VW - (reinterpret_cast<uintptr_t>(src) % VW)) % VW);
+            if (head > len) head = len;
+            const int64_t nvec = (len - head) / VW;
+            const int64_t body_end = head + nvec * VW;
+            const V *vs = reinterpret_cast<const V *>(src + head);
+            V *vd = reinterpret_cast<V *>(dst + head);
+            for (int64_t base = 0; base < nvec; base += (int64_t)kTGThreads * kTGUnroll) {
+                V reg[kTGUnroll];
 #pragma unroll
-            for (int k = 0; k < kTGUnroll; ++k) {
-                const int64_t idx = base + tid + (int64_t)k * kTGThreads;
-                if (idx < nvec) reg[k] = ld_stream(vs + idx);
-            }
+                for (int k = 0; k < kTGUnroll; ++k) {
+                    const int64_t idx = base + tid + (int64_t)k * kTGThreads;
+                    if (idx < nvec) reg[k] = ld_stream(vs + idx);
+                }
 #pragma unroll
-            for (int k = 0; k < kTGUnroll; ++k) {
-                const int64_t idx = base + tid + (int64_t)k * kTGThreads;
-                if (idx < nvec) vd[idx] = reg[k];
+                for (int k = 0; k < kTGUnroll; ++k) {
+                    const int64_t idx = base + tid + (int64_t)k * kTGThreads;
+                    if (idx < nvec) vd[idx] = reg[k];
+                }
             }
+            if (head > 0) copy_elems(dst, src, head, p.es, tid, kTGThreads);
+            if (len > body_end) copy_elems(dst + body_end, src + body_end, len - body_end, p.es, tid, kTGThreads);
+            lo += len;
         }
-        if (head > 0) copy_elems(dst, src, head, p.es, tid, kTGThreads);
-        if (len > body_end) copy_elems(dst + body_end, src + body_end, len - body_end, p.es, tid, kTGThreads);
-        lo += len;
+        if (stride == 0) break;
     }
 }
 
@@ -373,7 +384,13 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
         if (grid < 1) grid = 1;
         int64_t share = (total + grid - 1) / grid;
         share = (share + 15) / 16 * 16;
+        int64_t stride = 0;
+        if (TGC_TG_CHUNK > 0 && share > TGC_TG_CHUNK) {
+            share = (TGC_TG_CHUNK + 15) / 16 * 16;
+            stride = grid * share;
+        }
         grid = (total + share - 1) / share;
+        if (stride > 0 && grid > stride / share) grid = stride / share;
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -384,11 +401,11 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = TGC_TG_PDL ? 1 : 0;
         switch (vw) {
-            case 16: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<16>, p, share); break;
-            case 8: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<8>, p, share); break;
-            case 4: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<4>, p, share); break;
-            case 2: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<2>, p, share); break;
-            default: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<1>, p, share); break;
+            case 16: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<16>, p, share, stride); break;
+            case 8: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<8>, p, share, stride); break;
+            case 4: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<4>, p, share, stride); break;
+            case 2: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<2>, p, share, stride); break;
+            default: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<1>, p, share, stride); break;
         }
         if (e == cudaSuccess) e = cudaGetLastError();
         return e == cudaSuccess ? TGC_OK : cuda_fail(e);
