@@ -317,8 +317,7 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 #define TGC_TRACE_MMA_ACC_NS 9   /* MMA issuer: time waiting for a free accumulator  */
 #define TGC_TRACE_EPI_WAIT_NS 10 /* epilogue (first warp): time waiting for results  */
 #define TGC_TRACE_LOAD_STALL_NS 11 /* TMA issuer: time waiting for free stages       */
-#define TGC_TRACE_HELP_PIECES 12 /* tile loader: pieces it copied while its first tile
-                                    waited for remote data (start-up assist)         */
+                                 /* word 12 is unused                                */
 #define TGC_TRACE_COPY_WARPS 13  /* producer: warps of this CTA that took pieces     */
 
 /*

@@ -272,8 +272,8 @@ def test_trace_records_every_cta():
     assert used.shape[0] >= 2
     # both CTAs of a pair count each 256 x 256 tile they share
     assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
-    # every piece is copied once, by a producer warp or by a tile loader's start-up assist
-    copied = int(used[:, _lib.TRACE["pieces"]].sum()) + int(used[:, _lib.TRACE["help_pieces"]].sum())
+    # every piece is copied once, by one of the producer warps
+    copied = int(used[:, _lib.TRACE["pieces"]].sum())
     assert copied == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
     assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])
 

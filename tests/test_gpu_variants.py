@@ -1,0 +1,103 @@
+"""The library's non-default compile-time paths, built once into a separate
+library under the package's build folder and checked like the default build:
+
+- TGC_COPY_LSU=0: the fused kernel's producer is one warp of bulk async copies
+  (global -> shared -> global through four slots) instead of register copies;
+- TGC_TG_CHUNK=0: the flat TGATHER kernel gives each CTA one contiguous share
+  instead of dealing 32 KiB chunks round-robin.
+
+Results must be identical to the oracle (TGATHER bit for bit, GEMM within the
+tolerance, bit for bit on integer-exact inputs) and to the default build's
+unfused path.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tile_gather_comm_gb300 as tgc
+from tile_gather_comm_gb300 import _build, _lib
+from tile_gather_comm_gb300.workloads import TG_CONFIGS, make_tg_inputs
+
+from .helpers import assert_within_tol, bits16, requires_gpu
+from .test_gpu_ag_matmul import Run, _custom, _inputs, _oracle_full
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0}
+
+
+@pytest.fixture(scope="module")
+def variant_lib():
+    requires_gpu()
+    path = _build.build_variant(os.path.join(_build.PKG, "_build", "variant_bulk_copy"), VARIANT)
+    return _lib.load_library(path)
+
+
+@pytest.fixture
+def use_variant(variant_lib):
+    """Route the binding's calls to the variant build for the duration of a test."""
+    default = _lib.lib()
+    _lib._lib = variant_lib
+    try:
+        yield variant_lib
+    finally:
+        _lib._lib = default
+
+
+@pytest.mark.parametrize("pivot", ["page", "ready_queue"])
+def test_bulk_producer_tiny_all_ranks(use_variant, pivot):
+    cfg, shards, B = _inputs("tiny")
+    C_ref, a_ref = _oracle_full(shards, B)
+    run = Run(cfg, shards, B)
+    for rank in range(cfg.R):
+        run.C.fill_(float("nan"))
+        run.a.view(torch.int16).fill_(-1)  # a stale read of `a` shows up as NaN in C
+        run(pivot=pivot, rank=rank)
+        assert_within_tol(run.C, C_ref, f"bulk producer {pivot} rank {rank}")
+        assert np.array_equal(bits16(run.a), a_ref)
+
+
+def test_bulk_producer_integer_exact_and_trace(use_variant):
+    # integer values in {-2..2}, K = 64: every partial sum is exact, so C is exact
+    cfg, _, _ = _custom(4, 256, 64, 512, 64, seed=31)
+    g = torch.Generator().manual_seed(31)
+    shards = [torch.randint(-2, 3, (cfg.H, cfg.K), generator=g).to(torch.bfloat16) for _ in range(cfg.R)]
+    B = torch.randint(-2, 3, (cfg.N, cfg.K), generator=g).to(torch.bfloat16)
+    run = Run(cfg, shards, B)
+    trace = torch.zeros(152 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+    run(trace=trace)
+    exact = (torch.cat(shards).double() @ B.double().T).to(torch.bfloat16)
+    assert torch.equal(run.C.cpu(), exact)
+    t = trace.view(-1, _lib.TRACE_WORDS).cpu()
+    used = t[t[:, _lib.TRACE["start"]] > 0]
+    assert set(used[:, _lib.TRACE["copy_warps"]].tolist()) == {1}
+    assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
+
+
+def test_bulk_producer_matches_unfused_bitwise(use_variant):
+    # ragged: M not a multiple of the 256-row tile, N not a multiple of 256
+    cfg, shards, B = _custom(3, 200, 256, 328, 40, seed=32)
+    run = Run(cfg, shards, B)
+    run(mode="unfused")
+    ref = run.C.clone()
+    for pivot in ("page", "shard", "ready_queue"):
+        run.C.zero_()
+        run(pivot=pivot)
+        assert torch.equal(run.C, ref), pivot
+    assert torch.equal(run.a, torch.cat(run.shards))
+
+
+@pytest.mark.parametrize("name", ["bw_f16", "ragged_i32"])
+def test_one_share_tgather_bit_exact(use_variant, name):
+    cfg = TG_CONFIGS[name]
+    srcs = make_tg_inputs(cfg, seed=0)
+    D0, D1, D2, H, W = cfg.shape
+    dst = torch.empty((D0, D1, D2, cfg.nranks * H, W), dtype=cfg.dtype, device=DEV)
+    dst.view(torch.uint8).fill_(0xA5)
+    tgc.tgc_tgather(dst, [s.to(DEV) for s in srcs])
+    torch.cuda.synchronize()
+    ref = oracle.tgather([s.numpy() for s in srcs])
+    assert dst.cpu().numpy().tobytes() == ref.tobytes()

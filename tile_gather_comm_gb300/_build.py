@@ -46,10 +46,20 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    out_dir = os.path.join(PKG, "_build")
+    return _compile(os.path.join(PKG, "_build"), LIB, [], verbose, ptxas_info)
+
+
+def build_variant(out_dir: str, defines: dict) -> str:
+    """Build the library with compile-time settings changed (e.g. {"TGC_COPY_LSU": 0})
+    into out_dir/libtgc.so and return its path; the in-tree library is not touched."""
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    return _compile(out_dir, os.path.join(out_dir, "libtgc.so"), flags, False, False)
+
+
+def _compile(out_dir: str, lib_path: str, extra: list, verbose: bool, ptxas_info: bool) -> str:
     os.makedirs(out_dir, exist_ok=True)
     common = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]
+              "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC, *extra]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
@@ -65,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

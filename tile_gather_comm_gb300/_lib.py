@@ -36,8 +36,7 @@ DTYPES = {
 MAX_RANKS = 64
 TRACE_WORDS = 16
 TRACE = dict(start=0, wait_ns=1, waited_tiles=2, copy_first=3, copy_last=4, pieces=5, end=6, tiles=7,
-             mma_stage_ns=8, mma_acc_ns=9, epi_wait_ns=10, load_stall_ns=11, help_pieces=12,
-             copy_warps=13)
+             mma_stage_ns=8, mma_acc_ns=9, epi_wait_ns=10, load_stall_ns=11, copy_warps=13)
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -85,7 +84,14 @@ def lib() -> ctypes.CDLL:
         return _lib
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
-    L = ctypes.CDLL(LIB_PATH)
+    _lib = load_library(LIB_PATH)
+    return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library (the in-tree one, or one made by _build.build_variant)
+    and declare the C prototypes of its entry points."""
+    L = ctypes.CDLL(path)
     L.tgc_tgather.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _i64, _i64, _i64,
                               ctypes.c_int, _vp]
     L.tgc_tgather.restype = ctypes.c_int
@@ -115,7 +121,6 @@ def lib() -> ctypes.CDLL:
     L.tgc_last_cuda_error.restype = ctypes.c_int
     L.tgc_version.argtypes = []
     L.tgc_version.restype = ctypes.c_char_p
-    _lib = L
     return L
 
 

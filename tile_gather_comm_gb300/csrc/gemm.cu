@@ -133,19 +133,8 @@ constexpr int smem_bytes() {
            (SLOTS ? kSlots * kSlotBytes : 0) + 512 /* barriers + TMEM address */;
 }
 
-// Start-up assist: staging slots the tile loader carves out of its (still
-// empty) pipeline stages while its first tile waits for remote data.  Off by
-// default: measured on GB300 it slowed the fused MLP-up workload (0.656 vs
-// 0.609 ms) and the square one (0.126 vs 0.115 ms) -- each helping CTA must
-// drain up to 192 KiB of in-flight copies before its first tile, and the extra
-// copy traffic slows the CTAs that already compute their local tiles.
-#ifndef TGC_STARTUP_ASSIST
-#define TGC_STARTUP_ASSIST 0
-#endif
-constexpr int kHelpSlots = 24;
 static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<2, false>() <= 232448, "shared memory per CTA");
-static_assert((kHelpSlots + 2 * 6 + 4 + kSlots + 1) * 8 + 4 <= 512, "barrier area");
-static_assert(kHelpSlots * kSlotBytes <= 6 * (16384 + 16384), "assist slots fit in the pipeline stages");
+static_assert((2 * 8 + 4 + kSlots + 1) * 8 + 4 <= 512, "barrier area");
 
 struct GemmParams {
     int M, N, K;
@@ -191,7 +180,7 @@ struct GemmParams {
 constexpr int kTraceWords = 16;
 enum : int {
     kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles,
-    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrHelpPieces, kTrCopyWarps
+    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrCopyWarps = 13  // word 12 unused
 };
 
 // mbar_wait that adds the time it blocked to *acc (only when tracing).
@@ -306,23 +295,6 @@ __device__ int ring_row(const GemmParams &p, int idx, int lane, bool *waited) {
 
 // ---------------------------------------------------------------- roles
 
-template <int NSLOT, class Stop>
-__device__ uint32_t copy_loop(const GemmParams &p, uint8_t *slots, uint64_t *bars, Stop stop, bool *ok_out);
-
-// Lane-local, non-blocking: is the data of this CTA's rows of tile `tp` published?
-__device__ __forceinline__ bool tile_data_ready(const GemmParams &p, const TilePos &tp, uint32_t crank, int tile_m) {
-    if (tp.ring_idx >= 0) {
-        const uint64_t e = ld_acquire_gpu_u64(p.ring + tp.ring_idx);
-        return (uint32_t)(e >> 32) == p.epoch && (uint32_t)e != 0u;
-    }
-    const int m0 = tp.pid_m * tile_m + (int)crank * 128;
-    if (m0 >= p.M || (m0 >= p.local_row0 && m0 + 128 <= p.local_row1)) return true;
-    const int m1 = (m0 + 128) < p.M ? (m0 + 128) : p.M;
-    for (int b = m0 / p.cb; b <= (m1 - 1) / p.cb; ++b)
-        if (ld_acquire_gpu(p.progress + b) != p.epoch) return false;
-    return true;
-}
-
 // Cluster-tile index space: cluster c of nclusters persistent clusters (a
 // "cluster" is a single CTA when CG == 1).
 template <int CG>
@@ -333,7 +305,7 @@ __device__ __forceinline__ int num_clusters() { return (int)gridDim.x / CG; }
 template <int CG, bool FUSED, bool PROD>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
-                         uint64_t *helpbar, uint32_t crank, int lane) {
+                         uint32_t crank, int lane) {
     using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     uint32_t it = 0;
     bool ok = true;
@@ -341,27 +313,8 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     // completion of every stage is counted on the even CTA's full barrier
     const uint32_t full0 = CG == 2 ? mapa_shared(smem_addr(full), 0) : smem_addr(full);
     const uint64_t polA = make_policy(TGC_A_HINT), polB = make_policy(TGC_B_HINT);
-    uint32_t help_pieces = 0;
-    bool first = true;
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>()) {
         TilePos tp = tile_at(p, t);
-        if (TGC_STARTUP_ASSIST && FUSED && PROD && first) {
-            // Start-up assist: while this CTA's first tile waits for remote data,
-            // its pipeline stages are empty; copy pieces through them until the
-            // data is published, then drain and start the GEMM.
-            first = false;
-            bool help = false;
-            if (lane == 0) help = !tile_data_ready(p, tp, crank, C::kTileM);
-            help = __shfl_sync(0xffffffffu, help ? 1 : 0, 0) != 0;
-            if (help) {
-                bool hok = true;
-                if (lane == 0)
-                    help_pieces = copy_loop<kHelpSlots>(
-                        p, sA, helpbar, [&] { return tile_data_ready(p, tp, crank, C::kTileM); }, &hok);
-                hok = __shfl_sync(0xffffffffu, hok ? 1 : 0, 0) != 0;
-                if (!hok) { ok = false; break; }
-            }
-        }
         if (tp.ring_idx >= 0) {
             bool spun = false;
             const uint64_t w0 = p.trace != nullptr ? globaltimer_ns() : 0;
@@ -420,7 +373,6 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         p.trace[blockIdx.x * kTraceWords + kTrWaitNs] = wait_ns;
         p.trace[blockIdx.x * kTraceWords + kTrWaitedTiles] = waited_tiles;
         p.trace[blockIdx.x * kTraceWords + kTrLoadStallNs] = load_stall_ns;
-        p.trace[blockIdx.x * kTraceWords + kTrHelpPieces] = help_pieces;
     }
     if (!ok && lane == 0) {
         if (CG == 1 || crank == 0) {
@@ -625,23 +577,24 @@ __device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticke
     }
 }
 
-// Copy loop (one lane).  Work arrives in pieces of up to kPieceBytes, handed
-// out by a global ticket (any resident CTA can copy any block), and flows
-// through NSLOT shared-memory slots of kSlotBytes as sub-copies: bulk load
+// Bulk copy loop (one lane; TGC_COPY_LSU=0).  Work arrives in pieces of up to
+// kPieceBytes, handed out by a global ticket (any resident CTA can copy any
+// block), and flows through NSLOT shared-memory slots of kSlotBytes as
+// sub-copies: bulk load
 // global -> slot, then bulk store slot -> `a`.  A slot is reused as soon as its
 // store has finished READING shared memory, while the store's global writes
 // may still be in flight.  A piece is retired -- counted toward its block, and
 // the block published by the piece that completes it -- once the writes of its
 // last sub-copy have landed, which may lag up to kStoreLag stores behind, so
-// loads, stores in flight and retirement overlap.  `stop()` is asked before
-// each new piece; once it is true (or no ticket is left) the loop finishes the
-// pieces it holds, waits for all its copies, retires them and returns the
-// number of pieces it retired.  *ok becomes false if a wait was abandoned.
+// loads, stores in flight and retirement overlap.  Once no ticket is left the
+// loop finishes the pieces it holds, waits for all its copies, retires them and
+// returns the number of pieces it retired.  *ok becomes false if a wait was
+// abandoned.
 constexpr int kStoreLag = 6;
 constexpr int kPieceRing = 16;  // pieces loaded but not yet retired
 
-template <int NSLOT, class Stop>
-__device__ uint32_t copy_loop(const GemmParams &p, uint8_t *slots, uint64_t *bars, Stop stop, bool *ok_out) {
+template <int NSLOT>
+__device__ uint32_t copy_loop(const GemmParams &p, uint8_t *slots, uint64_t *bars, bool *ok_out) {
     const uint32_t total = (uint32_t)p.n_order * (uint32_t)p.pieces_per_block;
     // sub-copy sequence numbers: [0, tail) loads issued, [0, head) stores issued
     uint32_t head = 0, tail = 0;
@@ -660,7 +613,6 @@ __device__ uint32_t copy_loop(const GemmParams &p, uint8_t *slots, uint64_t *bar
         while (tail - head < (uint32_t)NSLOT) {
             if (!have_cur) {
                 if (nomore || pload - pret >= (uint32_t)kPieceRing) break;
-                if (stop()) { nomore = true; break; }
                 const uint32_t tk = atom_add_relaxed_gpu(p.tickets, 1u);
                 if (tk >= total) { nomore = true; break; }
                 cur = piece_of(p, tk);
@@ -743,7 +695,7 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
     if (lane != 0) return;
     const uint64_t t_first = p.trace != nullptr ? globaltimer_ns() : 0;
     bool ok = true;
-    const uint32_t pieces = copy_loop<kSlots>(p, sSlot, slotbar, [] { return false; }, &ok);
+    const uint32_t pieces = copy_loop<kSlots>(p, sSlot, slotbar, &ok);
     if (p.trace != nullptr) {
         p.trace[blockIdx.x * kTraceWords + kTrCopyFirst] = t_first;
         p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = globaltimer_ns();
@@ -848,8 +800,7 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *slotbar = tempty + 2;
     uint64_t *drain = slotbar + kSlots;
-    uint64_t *helpbar = drain + 1;  // kHelpSlots barriers of the start-up assist
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(helpbar + kHelpSlots);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;
@@ -859,7 +810,6 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], C::kEpiArrivals); }
         for (int i = 0; i < kSlots; ++i) mbar_init(&slotbar[i], 1);
         mbar_init(drain, 1);
-        for (int i = 0; i < kHelpSlots; ++i) mbar_init(&helpbar[i], 1);
         fence_mbarrier_init();
         fence_proxy_async_shared();
     }
@@ -878,7 +828,7 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        role_tma<CG, FUSED, PROD>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, helpbar, crank, lane);
+        role_tma<CG, FUSED, PROD>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
         role_mma<CG, FUSED, PROD>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
     } else if (warp == 2 || warp == 3 || warp >= 8) {
