@@ -371,6 +371,7 @@ def run_ours(args, dist: Dist):
         res["e2e"] = bench_e2e(cfg, shards_h, B_h, a, progress, ws, order, delay, dev, stream, dist, args)
         if dist.rank == 0 and dist.world == 1:
             res["cpu_baseline"] = cpu_baseline(cfg, shards_h, B_h)
+            res["cpu_baseline_tgather"] = cpu_baseline_tgather(TG_CONFIGS["bw_f16"])
     del shards, B, C, a
     torch.cuda.empty_cache()
     return res
@@ -552,7 +553,10 @@ def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     sh = [bits(s) for s in shards_h]
     Bb = bits(B_h)
-    rows = sample_rows(cfg, seed=0, per_block_random=0)
+    # about 10 s of host work at the large workload's size: every comm block's first and last
+    # row plus seeded random rows of each block
+    per_block = max(0, (2048 // max(1, cfg.nblocks)) - 2)
+    rows = sample_rows(cfg, seed=0, per_block_random=per_block)
     if target_rows is not None:
         rows = rows[:target_rows]
     t0 = time.perf_counter()
@@ -561,8 +565,26 @@ def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):
     fl = 2.0 * len(rows) * cfg.N * cfg.K
     return {"value": round(fl / dt * 1e-12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"{len(rows)} rows of C (first and last row of each of the {cfg.nblocks} comm blocks), "
-                      f"all {cfg.N} columns, full K={cfg.K}; fp32 sequential-k dot products, OpenMP over rows"}
+            "sample": f"{len(rows)} rows of C (first and last row of each of the {cfg.nblocks} comm blocks plus "
+                      f"{per_block} seeded random rows of each), all {cfg.N} columns, full K={cfg.K}; "
+                      f"fp32 sequential-k dot products, OpenMP over rows"}
+
+
+def cpu_baseline_tgather(tcfg, reps: int = 5):
+    """The TGATHER oracle (element-wise byte copy) on the full workload, host cores."""
+    import oracle
+    from tile_gather_comm_gb300.workloads import make_tg_inputs
+
+    oracle.build()
+    srcs = [s.numpy() for s in make_tg_inputs(tcfg, seed=0)]
+    oracle.tgather(srcs)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.tgather(srcs)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(tcfg.bytes_moved / dt * 1e-9, 2), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt * reps, 3),
+            "sample": f"the full {tcfg.name} workload ({tcfg.bytes_moved} bytes read + written), {reps} runs"}
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
