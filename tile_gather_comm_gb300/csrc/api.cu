@@ -193,8 +193,9 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
                 seen[(size_t)c] = 1;
             }
         }
-        // pieces per block * blocks must fit the 32-bit ticket dispenser
-        const int64_t pieces = (a.comm_block_rows * a.K * 2 + 8191) / 8192;
+        // pieces per block * blocks must fit the 32-bit ticket dispenser (with room for
+        // the one ticket each copy warp draws past the end)
+        const int64_t pieces = (a.comm_block_rows * a.K * 2 + kPieceBytes - 1) / kPieceBytes;
         if (pieces * out.nblocks >= (int64_t(1) << 31)) return TGC_ERR_INVALID_ARG;
     }
     if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;

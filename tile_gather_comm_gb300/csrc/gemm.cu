@@ -105,7 +105,6 @@ template <bool FUSED, bool PROD>
 constexpr int kThreadsOf = (FUSED && PROD && TGC_COPY_LSU && kCopyWarps > 2) ? 32 * (6 + kCopyWarps) : kThreads;
 constexpr int kSlots = TGC_COPY_SLOTS;
 constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
-constexpr int kPieceBytes = 65536;      // unit of the ticket dispenser and of block completion
 constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns x 128 lanes
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 

@@ -16,6 +16,7 @@ namespace tgc {
 constexpr int kBN = 256;     // GEMM tile cols (tcgen05 N)
 constexpr int kBK = 64;      // bf16 elements per 128-byte swizzled row
 constexpr int kTileM = 256;  // GEMM tile rows: a pair of CTAs, 128 rows each (tcgen05 cta_group::2)
+constexpr int kPieceBytes = 65536;  // fused producer: unit of the ticket dispenser and of block completion
 
 // Records a CUDA error for tgc_last_cuda_error() and maps it to a status.
 int cuda_fail(cudaError_t e);
