@@ -41,7 +41,8 @@ METRIC = "fused AG-MatMul TFLOP/s (% BF16 peak); TGATHER GB/s (% HBM peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["tile_gather_comm_gb300/csrc/gemm.cu", "tile_gather_comm_gb300/csrc/prims.cuh",
                   "tile_gather_comm_gb300/csrc/schedule.h", "tile_gather_comm_gb300/csrc/internal.h"]
-TGATHER_SOURCES = ["tile_gather_comm_gb300/csrc/tgather.cu", "tile_gather_comm_gb300/csrc/prims.cuh"]
+TGATHER_SOURCES = ["tile_gather_comm_gb300/csrc/tgather.cu", "tile_gather_comm_gb300/csrc/prims.cuh",
+                   "tile_gather_comm_gb300/csrc/internal.h"]
 
 
 def parse_args(argv=None):
