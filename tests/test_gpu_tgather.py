@@ -60,6 +60,26 @@ def test_page_test_table(case, nranks):
     assert np.all(dst.cpu().numpy()[0, 0, 0, nranks * rows:].astype(np.int64) % 256 == 255)
 
 
+@pytest.mark.parametrize("case", [c for c in _golden_cases() if c[4] > 0], ids=lambda c: c[0])
+@pytest.mark.parametrize("nranks", [2, 8])
+def test_page_chunk_cases_with_release(case, nranks):
+    """The page's chunked scenarios (rows moved tile by tile, `page_tile_rows` rows at a time):
+    here each tile of rows is one progress chunk, released once its bytes are in place."""
+    name, dt, rows, cols, tile_rows = case
+    srcs = _tagged_sources(dt, rows, cols, nranks)
+    S = rows // tile_rows
+    progress = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    counters = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    dst = torch.full((1, 1, 1, nranks * rows, cols), -1, dtype=torch.from_numpy(srcs[0]).dtype, device=DEV)
+    for epoch in (1, 2):  # a second call over the same flags and counters
+        dst.fill_(-1)
+        tgc.tgc_tgather_ex(dst, [torch.from_numpy(s).to(DEV) for s in srcs], progress=progress,
+                           counters=counters, chunk_rows=tile_rows, epoch=epoch)
+        torch.cuda.synchronize()
+        assert _bytes(dst) == oracle.tgather(srcs).tobytes(), (name, epoch)
+        assert torch.all(progress == epoch) and torch.all(counters == 0)
+
+
 @pytest.mark.parametrize("shape", [(2, 3, 2, 5, 7), (1, 1, 1, 1, 1), (3, 1, 2, 33, 65), (1, 2, 1, 257, 129),
                                    (2, 1, 1, 1024, 24)])
 @pytest.mark.parametrize("dtype", [torch.uint8, torch.float16, torch.int32, torch.float64])
