@@ -24,6 +24,7 @@ Multi-GPU: the path does not shard; --gpus N runs N independent replicas
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -55,7 +56,7 @@ def parse_args(argv=None):
     p.add_argument("--quick", action="store_true", help="main line only: skip extras, e2e and cpu baseline")
     p.add_argument("--only", choices=["all", "tgather"], default="all",
                    help="tgather: time only the TGATHER workloads (small footprint, for profiling)")
-    p.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling period")
+    p.add_argument("--clock-ms", type=int, default=20, help="nvidia-smi sampling period")
     return p.parse_args(argv)
 
 
@@ -138,7 +139,7 @@ def profiled_traffic(summary_name: str, sources, per_launch_units: float | None 
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled while the timed regions run."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -160,7 +161,9 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self):
+    def stop(self, window: tuple | None = None):
+        """Summary of the samples.  `window` = (t0, t1) in time.time() seconds: the
+        region whose clocks `sm_mhz` reports (all samples under load if none fell in it)."""
         if self.proc is None:
             return None
         time.sleep(0.2)
@@ -169,26 +172,39 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4], parts[5:9]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        pmax = max(r[2] for r in rows)
-        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows  # power draw marks the samples under load
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[4]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "samples_under_load": len(loaded),
-                "reasons": reasons}
+        return clock_summary(lines, window)
+
+
+def clock_summary(lines, window: tuple | None = None):
+    """Summary of nvidia-smi CSV lines in ClockSampler.QUERY order: the median SM clock of
+    the samples inside `window` (host time.time() seconds), else of the samples under load
+    (power draw at least half the largest seen); the largest clocks and power; and every
+    throttle reason seen active in those samples."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append((float(parts[2]), float(parts[3]), float(parts[4]), parts[5], parts[6:10], ts))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    pmax = max(r[2] for r in rows)
+    loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows  # power draw marks the samples under load
+    inside = [r for r in rows if window is not None and window[0] <= r[5] <= window[1]]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in loaded + inside for i, v in enumerate(r[4]) if v.lower() == "active"})
+    return {"sm_mhz": statistics.median(r[0] for r in (inside or loaded)), "sm_max_mhz": max(r[1] for r in rows),
+            "power_w_max": max(r[2] for r in rows), "samples": len(rows), "samples_under_load": len(loaded),
+            "samples_in_value_region": len(inside),
+            "sm_mhz_under_load_all_regions": statistics.median(r[0] for r in loaded),
+            "reasons": reasons}
 
 
 def time_interleaved(variants: dict, steps: int, dist: Dist, stream, rounds: int = 6):
@@ -215,10 +231,13 @@ def time_interleaved(variants: dict, steps: int, dist: Dist, stream, rounds: int
     return {n: statistics.median(v) for n, v in times.items()}
 
 
-def time_device(fn, steps: int, warmup: int, dist: Dist, stream, per_step: list | None = None):
+def time_device(fn, steps: int, warmup: int, dist: Dist, stream, per_step: list | None = None,
+                wall: list | None = None):
     """Barrier + sync, then CUDA events on `stream` around exactly `steps` calls.
     If `per_step` is a list, an event is also recorded after every call and the
-    per-call times (ms) are appended to it."""
+    per-call times (ms) are appended to it.  If `wall` is a list, its two entries
+    become the host times (time.time()) just before the first call and after the
+    closing synchronize."""
     import torch
     for _ in range(warmup):
         fn()
@@ -226,6 +245,8 @@ def time_device(fn, steps: int, warmup: int, dist: Dist, stream, per_step: list 
     dist.barrier()
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step is not None else 2)]
+    if wall is not None:
+        wall[0] = time.time()
     ev[0].record(stream)
     for i in range(steps):
         fn()
@@ -233,6 +254,8 @@ def time_device(fn, steps: int, warmup: int, dist: Dist, stream, per_step: list 
             ev[i + 1].record(stream)
     ev[-1].record(stream)
     torch.cuda.synchronize()
+    if wall is not None:
+        wall[1] = time.time()
     dist.barrier()
     if per_step is not None:
         per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
@@ -304,7 +327,9 @@ def run_ours(args, dist: Dist):
 
     launches[0] = 0
     step_ms = []
-    ms_fused = time_device(lambda: call("fused"), args.steps, args.warmup, dist, stream, per_step=step_ms)
+    t_value = [0.0, 0.0]
+    ms_fused = time_device(lambda: call("fused"), args.steps, args.warmup, dist, stream, per_step=step_ms,
+                           wall=t_value)
     fused_launches_timed = args.steps  # one kernel per fused call
     value, ms_max = aggregate(ms_fused, flops, dist)
     kernel_tflops = flops / (ms_fused * 1e-3) * 1e-12
@@ -365,7 +390,7 @@ def run_ours(args, dist: Dist):
         res["tgather_context_long"] = bench_tgather(long_cfg, dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_context_long"]["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the "
                                                "TGATHER workload; per-launch start and drain amortised")
-    res["clocks"] = sampler.stop()
+    res["clocks"] = sampler.stop(window=tuple(t_value))
 
     if not args.quick:
         res["other_workloads"] = bench_other_workloads(dev, stream, dist, args, peaks)

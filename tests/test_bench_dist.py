@@ -74,3 +74,30 @@ def test_percentiles_nearest_rank():
     assert bench.percentiles([]) == {}
     # order of the input does not matter
     assert bench.percentiles([9, 1, 5, 3, 7]) == bench.percentiles([1, 3, 5, 7, 9]) == {"p10": 1, "p50": 5, "p90": 9}
+
+
+def test_clock_summary_window_and_reasons():
+    import datetime
+
+    import bench
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def line(dt_ms, mhz, watts, cap="Not Active", thermal="Not Active"):
+        ts = (t0 + datetime.timedelta(milliseconds=dt_ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {mhz}, 2070, {watts}, 0x0, Not Active, Not Active, {thermal}, {cap}\n"
+
+    lines = [line(0, 2070, 100), line(100, 1500, 1300, cap="Active"), line(200, 1400, 1350, cap="Active"),
+             line(300, 1800, 900), line(400, 2070, 120), "garbage\n"]
+    base = t0.timestamp()
+    s = bench.clock_summary(lines, window=(base + 0.05, base + 0.25))
+    assert s["samples"] == 5 and s["samples_in_value_region"] == 2
+    assert s["sm_mhz"] == 1450.0                     # median of the two samples inside the window
+    assert s["samples_under_load"] == 3              # power >= half of the 1350 W maximum
+    assert s["sm_mhz_under_load_all_regions"] == 1500.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1350.0 and s["sm_max_mhz"] == 2070.0
+    # no sample in the window: fall back to the samples under load
+    s2 = bench.clock_summary(lines, window=(base + 10, base + 11))
+    assert s2["samples_in_value_region"] == 0 and s2["sm_mhz"] == 1500.0
+    s3 = bench.clock_summary([line(0, 1000, 500, thermal="Active")])
+    assert s3["reasons"] == ["sw_thermal_slowdown"]
+    assert bench.clock_summary(["garbage\n"]) is None
