@@ -314,12 +314,12 @@ def run_ours(args, dist: Dist):
     epoch = [0]
     launches = [0]
 
-    def call(mode="fused", delays=True, pivot="page"):
+    def call(mode="fused", delays=True, pivot="page", out=None, out_format="bf16"):
         epoch[0] += 1
-        tgc.tgc_ag_matmul_ex(shards, B, C, a, cfg.cb, mode=mode, progress=progress, epoch=epoch[0],
-                             workspace=ws, order=order if mode == "fused" else None,
+        tgc.tgc_ag_matmul_ex(shards, B, C if out is None else out, a, cfg.cb, mode=mode, progress=progress,
+                             epoch=epoch[0], workspace=ws, order=order if mode == "fused" else None,
                              delay_ns=delay if (mode == "fused" and delays) else None, stream=stream,
-                             pivot=pivot)
+                             pivot=pivot, out_format=out_format)
         launches[0] += 2 if mode == "unfused" else 1
 
     sampler = ClockSampler(dist.local_rank, args.clock_ms)
@@ -362,9 +362,12 @@ def run_ours(args, dist: Dist):
 
         def cublas():  # context only: the vendor library GEMM on the gathered A, same shapes
             torch.matmul(a_full, B.T, out=C)
+        C8 = torch.empty(cfg.M, cfg.N, dtype=torch.uint8, device=dev)
         variants = {"fused": lambda: call("fused"), "unfused": lambda: call("unfused"),
                     "mm_only": lambda: call("mm_only"),
                     "ready_queue": lambda: call("fused", pivot="ready_queue"),
+                    "fused_ce": lambda: call("fused_ce"),
+                    "fused_fp8_out": lambda: call("fused", out=C8, out_format="f8e4m3"),
                     "cublas_gemm": cublas}
         if cfg.skewed:
             variants["no_delay"] = lambda: call("fused", delays=False)
@@ -378,7 +381,10 @@ def run_ours(args, dist: Dist):
         res["ready_queue"]["note"] = "same workload, READY_QUEUE tile order"
         res["cublas_gemm"]["note"] = ("context: torch.matmul (cuBLAS) on the already gathered A, "
                                       "same shapes; not part of this library")
-        del a_full
+        res["fused_ce"]["note"] = ("same workload, copy-engine producer: cudaMemcpyAsync per block on library "
+                                   "side streams + a stream write of its flag; default release order, no delays")
+        res["fused_fp8_out"]["note"] = "same workload and release schedule, C written as saturating float8 e4m3"
+        del a_full, C8
         res["fused_over_unfused"] = round(med["unfused"] / med["fused"], 4)
         res["comparison_timing"] = "interleaved rounds (6), median per variant"
         res["tgather"] = bench_tgather(TG_CONFIGS["bw_f16"], dev, stream, dist, peaks, peaks_kind, args)
@@ -390,6 +396,7 @@ def run_ours(args, dist: Dist):
         res["tgather_context_long"] = bench_tgather(long_cfg, dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_context_long"]["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the "
                                                "TGATHER workload; per-launch start and drain amortised")
+        res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
     res["clocks"] = sampler.stop(window=tuple(t_value))
 
     if not args.quick:
@@ -438,6 +445,57 @@ def bench_other_workloads(dev, stream, dist, args, peaks):
         line["config"] = f"{cfg.R} x ({cfg.H},{cfg.K}) shards, B ({cfg.N},{cfg.K}), cb={cfg.cb}"
         out[name] = line
         del shards, B, C, a
+    return out
+
+
+def bench_tgather_strided(tcfg, dev, dist, peaks, peaks_kind, pad: int = 64):
+    """tgc_tgather_strided on the TGATHER workload's sizes with every source a view of
+    rows padded by `pad` elements (row pitch W + pad) and the destination a view of a
+    padded buffer too, graph-replayed over rotating buffer sets > 4 x L2."""
+    import torch
+
+    import tile_gather_comm_gb300 as tgc
+    from tile_gather_comm_gb300.workloads import make_tg_inputs
+
+    srcs_h = make_tg_inputs(tcfg, seed=0)
+    D0, D1, D2, H, W = tcfg.shape
+    per_set = tcfg.bytes_moved
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, -(-4 * l2 // per_set))
+    sets = []
+    for _ in range(nsets):
+        srcs = []
+        for s in srcs_h:
+            buf = torch.empty((D0, D1, D2, H, W + pad), dtype=tcfg.dtype, device=dev)
+            buf[..., :W].copy_(s.to(dev))
+            srcs.append(buf[..., :W])
+        dbuf = torch.empty((D0, D1, D2, tcfg.nranks * H, W + pad), dtype=tcfg.dtype, device=dev)
+        sets.append((dbuf[..., :W], srcs))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for dst, srcs in sets:
+            tgc.tgc_tgather_strided(dst, srcs, stream=s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for dst, srcs in sets:
+                tgc.tgc_tgather_strided(dst, srcs, stream=s)
+    torch.cuda.synchronize()
+    reps = max(3, -(-400 // nsets))
+    ms = time_device(lambda: g.replay(), reps, 3, dist, torch.cuda.current_stream()) / nsets
+    gbs, _ = aggregate(ms, per_set, dist, scale=1e-9)
+    per_gpu = per_set / (ms * 1e-3) * 1e-9
+    out = {
+        "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(ms * 1e3, 3),
+        "config": f"{tcfg.nranks} x {str(tcfg.dtype).replace('torch.', '')} {tcfg.shape} views with row pitch "
+                  f"W+{pad} -> a destination view with row pitch W+{pad}",
+        "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
+        "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<16>"},
+    }
+    del sets, g
     return out
 
 

@@ -231,11 +231,12 @@ __global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams
 }
 
 // Strided views ("CANN PTO-ISA TGATHER 指令深度解析", §7.3 and §8.1: GlobalTensor
-// views with a shape and a stride, shared by every source).  Thread g of the
-// grid copies vector g of the flattened (row, vector) space; rows are ordered
-// (rank, d0, d1, d2, i), so consecutive threads touch consecutive vectors of
-// one row.  INNER = rows are contiguous in source and destination (VW-byte
-// vectors); otherwise every element is copied on its own with both inner strides.
+// views with a shape and a stride, shared by every source).  Rows are ordered
+// (rank, d0, d1, d2, i).  When rows are contiguous in source and destination
+// they are copied with VW-byte vectors by tgather_strided_rows_kernel (below);
+// otherwise tgather_strided_elems_kernel copies every element on its own with
+// both inner strides, thread g of the grid taking element g of the flattened
+// (row, element) space.
 struct TGStridedParams {
     const uint8_t *srcs[TGC_MAX_RANKS];
     uint8_t *dst;
@@ -243,12 +244,12 @@ struct TGStridedParams {
     int64_t D0, D1, D2, H;
     int64_t ss[5], ds[5];  // byte strides
     int64_t rows;          // nranks * D0 * D1 * D2 * H
-    int64_t nv;            // vectors (INNER) or elements per row
+    int64_t nv;            // vectors (contiguous rows) or elements per row
 };
 
-template <int VW, bool INNER>
-__global__ void __launch_bounds__(256) tgather_strided_kernel(const TGStridedParams p) {
-    using V = typename VecT<VW>::T;
+template <int ES>
+__global__ void __launch_bounds__(256) tgather_strided_elems_kernel(const TGStridedParams p) {
+    using V = typename VecT<ES>::T;
     const int64_t total = p.rows * p.nv;
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = g / p.nv, v = g - row * p.nv;
@@ -262,10 +263,46 @@ __global__ void __launch_bounds__(256) tgather_strided_kernel(const TGStridedPar
         const int r = (int)(t / p.D0);
         const uint8_t *s = p.srcs[r] + d0 * p.ss[0] + d1 * p.ss[1] + d2 * p.ss[2] + i * p.ss[3];
         uint8_t *d = p.dst + d0 * p.ds[0] + d1 * p.ds[1] + d2 * p.ds[2] + ((int64_t)r * p.H + i) * p.ds[3];
-        if (INNER) {
-            *reinterpret_cast<V *>(d + v * VW) = ld_stream(reinterpret_cast<const V *>(s + v * VW));
-        } else {
-            *reinterpret_cast<V *>(d + v * p.ds[4]) = *reinterpret_cast<const V *>(s + v * p.ss[4]);
+        *reinterpret_cast<V *>(d + v * p.ds[4]) = *reinterpret_cast<const V *>(s + v * p.ss[4]);
+    }
+}
+
+// Strided views whose rows are contiguous in source and destination: one warp
+// copies one segment of one row, 32 x kTGUnroll vectors, with all its loads in
+// flight before its stores.  The row coordinates (rank, d0, d1, d2, i) are
+// decoded once per segment rather than once per vector.
+template <int VW>
+__global__ void __launch_bounds__(256) tgather_strided_rows_kernel(const TGStridedParams p, int64_t nseg) {
+    using V = typename VecT<VW>::T;
+    constexpr int kSeg = 32 * kTGUnroll;  // vectors per segment
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t items = p.rows * nseg;
+    for (int64_t it = (((int64_t)blockIdx.x * blockDim.x) + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int64_t row = it / nseg;
+        const int64_t v0 = (it - row * nseg) * kSeg;
+        int64_t t = row / p.H;
+        const int64_t i = row - t * p.H;
+        const int64_t d2 = t % p.D2;
+        t /= p.D2;
+        const int64_t d1 = t % p.D1;
+        t /= p.D1;
+        const int64_t d0 = t % p.D0;
+        const int r = (int)(t / p.D0);
+        const V *s = reinterpret_cast<const V *>(p.srcs[r] + d0 * p.ss[0] + d1 * p.ss[1] + d2 * p.ss[2] +
+                                                 i * p.ss[3]);
+        V *d = reinterpret_cast<V *>(p.dst + d0 * p.ds[0] + d1 * p.ds[1] + d2 * p.ds[2] +
+                                     ((int64_t)r * p.H + i) * p.ds[3]);
+        V reg[kTGUnroll];
+#pragma unroll
+        for (int j = 0; j < kTGUnroll; ++j) {
+            const int64_t v = v0 + j * 32 + lane;
+            if (v < p.nv) reg[j] = ld_stream(s + v);
+        }
+#pragma unroll
+        for (int j = 0; j < kTGUnroll; ++j) {
+            const int64_t v = v0 + j * 32 + lane;
+            if (v < p.nv) d[v] = reg[j];
         }
     }
 }
@@ -305,26 +342,32 @@ int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int64_t total = p.rows * p.nv;
-    int64_t grid = (total + 255) / 256;
     const int64_t cap = (int64_t)sm_count(dev) * 8;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    const dim3 gd((unsigned)grid), bd(256);
     if (inner) {
+        const int64_t seg = 32 * kTGUnroll;
+        const int64_t nseg = (p.nv + seg - 1) / seg;
+        int64_t grid = (p.rows * nseg + 7) / 8;  // 8 warps per CTA, one item each per pass
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        const dim3 gd((unsigned)grid), bd(256);
         switch (vw) {
-            case 16: tgather_strided_kernel<16, true><<<gd, bd, 0, stream>>>(p); break;
-            case 8: tgather_strided_kernel<8, true><<<gd, bd, 0, stream>>>(p); break;
-            case 4: tgather_strided_kernel<4, true><<<gd, bd, 0, stream>>>(p); break;
-            case 2: tgather_strided_kernel<2, true><<<gd, bd, 0, stream>>>(p); break;
-            default: tgather_strided_kernel<1, true><<<gd, bd, 0, stream>>>(p); break;
+            case 16: tgather_strided_rows_kernel<16><<<gd, bd, 0, stream>>>(p, nseg); break;
+            case 8: tgather_strided_rows_kernel<8><<<gd, bd, 0, stream>>>(p, nseg); break;
+            case 4: tgather_strided_rows_kernel<4><<<gd, bd, 0, stream>>>(p, nseg); break;
+            case 2: tgather_strided_rows_kernel<2><<<gd, bd, 0, stream>>>(p, nseg); break;
+            default: tgather_strided_rows_kernel<1><<<gd, bd, 0, stream>>>(p, nseg); break;
         }
     } else {
+        const int64_t total = p.rows * p.nv;
+        int64_t grid = (total + 255) / 256;
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        const dim3 gd((unsigned)grid), bd(256);
         switch (es) {
-            case 8: tgather_strided_kernel<8, false><<<gd, bd, 0, stream>>>(p); break;
-            case 4: tgather_strided_kernel<4, false><<<gd, bd, 0, stream>>>(p); break;
-            case 2: tgather_strided_kernel<2, false><<<gd, bd, 0, stream>>>(p); break;
-            default: tgather_strided_kernel<1, false><<<gd, bd, 0, stream>>>(p); break;
+            case 8: tgather_strided_elems_kernel<8><<<gd, bd, 0, stream>>>(p); break;
+            case 4: tgather_strided_elems_kernel<4><<<gd, bd, 0, stream>>>(p); break;
+            case 2: tgather_strided_elems_kernel<2><<<gd, bd, 0, stream>>>(p); break;
+            default: tgather_strided_elems_kernel<1><<<gd, bd, 0, stream>>>(p); break;
         }
     }
     e = cudaGetLastError();
