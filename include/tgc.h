@@ -317,7 +317,7 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 #define TGC_TRACE_MMA_ACC_NS 9   /* MMA issuer: time waiting for a free accumulator  */
 #define TGC_TRACE_EPI_WAIT_NS 10 /* epilogue (first warp): time waiting for results  */
 #define TGC_TRACE_LOAD_STALL_NS 11 /* TMA issuer: time waiting for free stages       */
-                                 /* word 12 is unused                                */
+#define TGC_TRACE_PIECE_BYTES 12 /* producer: copy piece size chosen for the call    */
 #define TGC_TRACE_COPY_WARPS 13  /* producer: warps of this CTA that took pieces     */
 
 /*

@@ -63,6 +63,16 @@ def _oracle_full(shards, B):
     return oracle.ag_matmul([bits16(s) for s in shards], bits16(B))
 
 
+def _expected_pieces(cfg, used):
+    """Copy pieces of one call, from the piece size its trace records (one size per call,
+    a power of two from 16 to 64 KiB)."""
+    sizes = set(int(x) for x in used[:, _lib.TRACE["piece_bytes"]].tolist())
+    assert len(sizes) == 1, sizes
+    pb = sizes.pop()
+    assert pb in (16384, 32768, 65536), pb
+    return cfg.nblocks * -(-cfg.cb * cfg.K * 2 // pb)
+
+
 def _custom(R, H, K, N, cb, seed=0, sigma=1.0):
     cfg = AGConfig("custom", R=R, H=H, K=K, N=N, cb=cb, b_sigma=sigma)
     return (cfg,) + tuple(make_ag_inputs(cfg, seed=seed))
@@ -274,16 +284,18 @@ def test_trace_records_every_cta():
     assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
     # every piece is copied once, by one of the producer warps
     copied = int(used[:, _lib.TRACE["pieces"]].sum())
-    assert copied == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
+    assert copied == _expected_pieces(cfg, used)
     assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])
 
 
 def test_copy_intensity_follows_local_lead():
     """The producer runs on two warps when the caller's own tiles fill the first two waves of the
-    tile order, and on every copy warp when the first waves reach remote rows; C is the same."""
+    tile order, and on every copy warp when the first waves reach remote rows; the piece size is
+    the largest of 64 / 32 / 16 KiB that gives every copy warp two pieces; C is the same."""
     seen = {}
-    for label, R, H in (("lead", 2, 4096), ("urgent", 8, 512)):
-        cfg, shards, B = _custom(R, H, 64, 4096, 256, seed=21)
+    for label, R, H, K, N in (("lead", 2, 4096, 64, 4096), ("urgent", 8, 512, 64, 4096),
+                              ("lead_big_copy", 2, 4096, 4096, 2560)):
+        cfg, shards, B = _custom(R, H, K, N, 256, seed=21)
         run = Run(cfg, shards, B)
         run(mode="unfused")
         ref = run.C.clone()
@@ -296,8 +308,13 @@ def test_copy_intensity_follows_local_lead():
         warps = set(int(w) for w in used[:, _lib.TRACE["copy_warps"]].tolist())
         assert len(warps) == 1, (label, warps)
         seen[label] = warps.pop()
-        assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
-    assert 1 <= seen["lead"] <= 2
+        assert int(used[:, _lib.TRACE["pieces"]].sum()) == _expected_pieces(cfg, used)
+        pb = int(used[0, _lib.TRACE["piece_bytes"]])
+        warps_total = used.shape[0] * seen[label]
+        pieces = lambda size: cfg.nblocks * -(-cfg.cb * cfg.K * 2 // size)
+        expect = next((sz for sz in (65536, 32768) if pieces(sz) >= 2 * warps_total), 16384)
+        assert pb == expect, (label, pb, expect)
+    assert 1 <= seen["lead"] <= 2 and seen["lead_big_copy"] == seen["lead"]
     assert seen["urgent"] >= seen["lead"]
 
 

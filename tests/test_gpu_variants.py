@@ -22,7 +22,7 @@ from tile_gather_comm_gb300 import _build, _lib
 from tile_gather_comm_gb300.workloads import TG_CONFIGS, make_tg_inputs
 
 from .helpers import assert_within_tol, bits16, requires_gpu
-from .test_gpu_ag_matmul import Run, _custom, _inputs, _oracle_full
+from .test_gpu_ag_matmul import Run, _custom, _expected_pieces, _inputs, _oracle_full
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -74,7 +74,7 @@ def test_bulk_producer_integer_exact_and_trace(use_variant):
     t = trace.view(-1, _lib.TRACE_WORDS).cpu()
     used = t[t[:, _lib.TRACE["start"]] > 0]
     assert set(used[:, _lib.TRACE["copy_warps"]].tolist()) == {1}
-    assert int(used[:, _lib.TRACE["pieces"]].sum()) == cfg.nblocks * -(-cfg.cb * cfg.K * 2 // 65536)
+    assert int(used[:, _lib.TRACE["pieces"]].sum()) == _expected_pieces(cfg, used)
 
 
 def test_bulk_producer_matches_unfused_bitwise(use_variant):

@@ -36,7 +36,8 @@ DTYPES = {
 MAX_RANKS = 64
 TRACE_WORDS = 16
 TRACE = dict(start=0, wait_ns=1, waited_tiles=2, copy_first=3, copy_last=4, pieces=5, end=6, tiles=7,
-             mma_stage_ns=8, mma_acc_ns=9, epi_wait_ns=10, load_stall_ns=11, copy_warps=13)
+             mma_stage_ns=8, mma_acc_ns=9, epi_wait_ns=10, load_stall_ns=11, piece_bytes=12,
+             copy_warps=13)
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64

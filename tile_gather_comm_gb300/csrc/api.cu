@@ -195,7 +195,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
         }
         // pieces per block * blocks must fit the 32-bit ticket dispenser (with room for
         // the one ticket each copy warp draws past the end)
-        const int64_t pieces = (a.comm_block_rows * a.K * 2 + kPieceBytes - 1) / kPieceBytes;
+        const int64_t pieces = (a.comm_block_rows * a.K * 2 + kMinPieceBytes - 1) / kMinPieceBytes;
         if (pieces * out.nblocks >= (int64_t(1) << 31)) return TGC_ERR_INVALID_ARG;
     }
     if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;

@@ -154,6 +154,7 @@ struct GemmParams {
     int first_block;
     int n_order;
     int pieces_per_block;
+    int piece_bytes;      // copy piece size of this call
     int64_t row_bytes;
     int64_t block_bytes;
     const uint8_t *shards[TGC_MAX_RANKS];
@@ -179,7 +180,7 @@ struct GemmParams {
 constexpr int kTraceWords = 16;
 enum : int {
     kTrStart = 0, kTrWaitNs, kTrWaitedTiles, kTrCopyFirst, kTrCopyLast, kTrPieces, kTrEnd, kTrTiles,
-    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrCopyWarps = 13  // word 12 unused
+    kTrMmaStageNs, kTrMmaAccNs, kTrEpiWaitNs, kTrLoadStallNs, kTrPieceBytes, kTrCopyWarps
 };
 
 // mbar_wait that adds the time it blocked to *acc (only when tracing).
@@ -536,12 +537,12 @@ __device__ __forceinline__ Piece piece_of(const GemmParams &p, uint32_t ticket) 
                       ? p.order[pos]
                       : default_release_block(pos, p.nblocks, p.first_block, p.local_b0, p.local_b1);
     const int r = c / p.blocks_per_rank, s = c % p.blocks_per_rank;
-    const int64_t off = (int64_t)j * kPieceBytes;
+    const int64_t off = (int64_t)j * p.piece_bytes;
     const int64_t rem = p.block_bytes - off;
     Piece pc;
     pc.src = p.shards[r] + (int64_t)s * p.block_bytes + off;
     pc.dst = p.a + ((int64_t)r * p.rows_per_rank + (int64_t)s * p.cb) * p.row_bytes + off;
-    pc.bytes = (uint32_t)(rem < kPieceBytes ? rem : kPieceBytes);
+    pc.bytes = (uint32_t)(rem < p.piece_bytes ? rem : p.piece_bytes);
     pc.block = c;
     return pc;
 }
@@ -577,7 +578,7 @@ __device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticke
 }
 
 // Bulk copy loop (one lane; TGC_COPY_LSU=0).  Work arrives in pieces of up to
-// kPieceBytes, handed out by a global ticket (any resident CTA can copy any
+// p.piece_bytes, handed out by a global ticket (any resident CTA can copy any
 // block), and flows through NSLOT shared-memory slots of kSlotBytes as
 // sub-copies: bulk load
 // global -> slot, then bulk store slot -> `a`.  A slot is reused as soon as its
@@ -700,6 +701,7 @@ __device__ void role_copy(const GemmParams &p, uint8_t *sSlot, uint64_t *slotbar
         p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = globaltimer_ns();
         p.trace[blockIdx.x * kTraceWords + kTrPieces] = pieces;
         p.trace[blockIdx.x * kTraceWords + kTrCopyWarps] = 1;
+        p.trace[blockIdx.x * kTraceWords + kTrPieceBytes] = (uint64_t)p.piece_bytes;
     }
 }
 
@@ -775,6 +777,7 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
             p.trace[blockIdx.x * kTraceWords + kTrCopyLast] = last;
             p.trace[blockIdx.x * kTraceWords + kTrPieces] = sum;
             p.trace[blockIdx.x * kTraceWords + kTrCopyWarps] = (uint64_t)p.copy_warps;
+            p.trace[blockIdx.x * kTraceWords + kTrPieceBytes] = (uint64_t)p.piece_bytes;
         }
     }
 }
@@ -985,6 +988,21 @@ static int copy_warps_for(const GemmParams &p, int nclusters) {
     return urgent || kCopyWarps < 2 ? kCopyWarps : 2;
 }
 
+// Copy piece size: the largest power of two from kMaxPieceBytes down to
+// kMinPieceBytes that still gives every copy warp of the grid two pieces.  A
+// small gather spread over many warps then finishes in a few round trips
+// instead of one long piece per warp; a large one keeps the per-piece fence
+// and counter traffic low.
+static int piece_bytes_for(const GemmParams &p, int64_t copy_warps_total) {
+    int pb = kMaxPieceBytes;
+    while (pb > kMinPieceBytes) {
+        const int64_t pieces = (int64_t)p.n_order * ((p.block_bytes + pb - 1) / pb);
+        if (pieces >= 2 * copy_warps_total) break;
+        pb /= 2;
+    }
+    return pb;
+}
+
 int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     using C = Cfg<kCG, false>;  // tile geometry does not depend on FUSED
     GemmParams p;
@@ -1028,7 +1046,6 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.n_order = (int)L.n_order;
         p.row_bytes = L.K * 2;
         p.block_bytes = L.cb * L.K * 2;
-        p.pieces_per_block = (int)((p.block_bytes + kPieceBytes - 1) / kPieceBytes);
         for (int r = 0; r < L.nranks; ++r) p.shards[r] = static_cast<const uint8_t *>(L.shards[r]);
         p.a = static_cast<uint8_t *>(L.a);
         p.progress = L.progress;
@@ -1068,7 +1085,13 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
     if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
     if (nclusters < 1) nclusters = 1;
-    if (variant == 1) p.copy_warps = copy_warps_for(p, nclusters);
+    if (variant == 1) {
+        p.copy_warps = copy_warps_for(p, nclusters);
+        p.piece_bytes = piece_bytes_for(p, (int64_t)nclusters * kCG * p.copy_warps);
+    } else {
+        p.piece_bytes = kMaxPieceBytes;
+    }
+    if (L.fused) p.pieces_per_block = (int)((p.block_bytes + p.piece_bytes - 1) / p.piece_bytes);
     return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, p, nclusters, stream)
          : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, p, nclusters, stream)
                         : launch<kCG, true, false>(tmA, tmL, tmB, p, nclusters, stream);

@@ -16,7 +16,14 @@ namespace tgc {
 constexpr int kBN = 256;     // GEMM tile cols (tcgen05 N)
 constexpr int kBK = 64;      // bf16 elements per 128-byte swizzled row
 constexpr int kTileM = 256;  // GEMM tile rows: a pair of CTAs, 128 rows each (tcgen05 cta_group::2)
-constexpr int kPieceBytes = 65536;  // fused producer: unit of the ticket dispenser and of block completion
+// Fused producer: the unit of the ticket dispenser and of block completion is a
+// piece of kMinPieceBytes..kMaxPieceBytes, chosen per call (a power of two).
+#ifndef TGC_MIN_PIECE_BYTES
+#define TGC_MIN_PIECE_BYTES 16384
+#endif
+constexpr int kMaxPieceBytes = 65536;
+constexpr int kMinPieceBytes = TGC_MIN_PIECE_BYTES;
+static_assert(kMinPieceBytes >= 4096 && kMinPieceBytes <= kMaxPieceBytes && kMinPieceBytes % 16 == 0, "piece size");
 
 // Records a CUDA error for tgc_last_cuda_error() and maps it to a status.
 int cuda_fail(cudaError_t e);
