@@ -439,9 +439,10 @@ def bench_other_workloads(dev, stream, dist, args, peaks):
         med = time_interleaved({"fused": lambda: call("fused"),
                                 "fused_ready_queue": lambda: call("fused", "ready_queue"),
                                 "unfused": lambda: call("unfused"), "mm_only": lambda: call("mm_only")},
-                               max(args.steps, 60), dist, stream)
+                               max(args.steps, 300), dist, stream, rounds=10)
         line = {k: round(aggregate(v, float(cfg.flops), dist)[0], 1) for k, v in med.items()}
         line["unit"] = "TFLOP/s"
+        line["fused_ready_queue_over_unfused"] = round(med["unfused"] / med["fused_ready_queue"], 4)
         line["config"] = f"{cfg.R} x ({cfg.H},{cfg.K}) shards, B ({cfg.N},{cfg.K}), cb={cfg.cb}"
         out[name] = line
         del shards, B, C, a
