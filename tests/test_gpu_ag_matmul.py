@@ -408,3 +408,30 @@ def test_stress_random_orders_delays_pivots_bit_exact():
     ws = run.ws.cpu()
     assert torch.all(ws[:4] == 0) and torch.all(ws[64:80] == 0)
     assert torch.all(ws[128:128 + 4 * cfg.nblocks] == 0)
+
+
+def test_random_shapes_against_oracle():
+    """Seeded random problem shapes (ranks, shard rows, comm-block rows, K, N, rank, tile order,
+    mode) compared with the oracle element by element; the fused paths also bit for bit with
+    the unfused one and `a` with the concatenated shards."""
+    g = torch.Generator().manual_seed(2026)
+    pick = lambda seq: seq[int(torch.randint(0, len(seq), (1,), generator=g))]
+    for i in range(24):
+        R = pick([1, 2, 3, 4, 6, 8])
+        cb = pick([8, 16, 40, 64, 128, 256])
+        H = cb * pick([1, 2, 3, 5])
+        K = 8 * pick([1, 3, 8, 17, 64])
+        N = 8 * pick([1, 5, 32, 33, 96])
+        cfg, shards, B = _custom(R, H, K, N, cb, seed=100 + i)
+        C_ref, a_ref = _oracle_full(shards, B)
+        run = Run(cfg, shards, B)
+        run(mode="unfused")
+        ref = run.C.clone()
+        assert_within_tol(run.C, C_ref, f"shape {i}: R={R} H={H} cb={cb} K={K} N={N} unfused")
+        for mode, pivot in (("fused", pick(["page", "shard", "ready_queue"])), ("fused_ce", "page")):
+            rank = int(torch.randint(0, R, (1,), generator=g))
+            run.a.view(torch.int16).fill_(-1)
+            run.C.fill_(float("nan"))
+            run(mode=mode, pivot=pivot, rank=rank)
+            assert torch.equal(run.C, ref), (i, R, H, cb, K, N, mode, pivot, rank)
+            assert np.array_equal(bits16(run.a), a_ref), (i, mode)
