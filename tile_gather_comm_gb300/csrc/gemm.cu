@@ -580,16 +580,15 @@ __device__ __forceinline__ void retire_piece(const GemmParams &p, uint32_t ticke
 // Bulk copy loop (one lane; TGC_COPY_LSU=0).  Work arrives in pieces of up to
 // p.piece_bytes, handed out by a global ticket (any resident CTA can copy any
 // block), and flows through NSLOT shared-memory slots of kSlotBytes as
-// sub-copies: bulk load
-// global -> slot, then bulk store slot -> `a`.  A slot is reused as soon as its
-// store has finished READING shared memory, while the store's global writes
-// may still be in flight.  A piece is retired -- counted toward its block, and
-// the block published by the piece that completes it -- once the writes of its
-// last sub-copy have landed, which may lag up to kStoreLag stores behind, so
-// loads, stores in flight and retirement overlap.  Once no ticket is left the
-// loop finishes the pieces it holds, waits for all its copies, retires them and
-// returns the number of pieces it retired.  *ok becomes false if a wait was
-// abandoned.
+// sub-copies: bulk load global -> slot, then bulk store slot -> `a`.  A slot
+// is reused as soon as its store has finished READING shared memory, while the
+// store's global writes may still be in flight.  A piece is retired -- counted
+// toward its block, and the block published by the piece that completes it --
+// once the writes of its last sub-copy have landed, which may lag up to
+// kStoreLag stores behind, so loads, stores in flight and retirement overlap.
+// Once no ticket is left the loop finishes the pieces it holds, waits for all
+// its copies, retires them and returns the number of pieces it retired.  *ok
+// becomes false if a wait was abandoned.
 constexpr int kStoreLag = 6;
 constexpr int kPieceRing = 16;  // pieces loaded but not yet retired
 
