@@ -101,3 +101,15 @@ def test_clock_summary_window_and_reasons():
     s3 = bench.clock_summary([line(0, 1000, 500, thermal="Active")])
     assert s3["reasons"] == ["sw_thermal_slowdown"]
     assert bench.clock_summary(["garbage\n"]) is None
+
+
+def test_strip_comments_keeps_code_and_literals():
+    import bench
+    src = ('int a = 1; // trailing\n/* block\n   comment */ const char *s = "x//y/*z*/";\n'
+           "char q = '\"'; char e = '\\\\';\n\n   int b;   // c\n")
+    out = bench.strip_comments(src)
+    assert out.splitlines() == ['int a = 1;', 'const char *s = "x//y/*z*/";', "char q = '\"'; char e = '\\\\';",
+                                'int b;']
+    # comment and whitespace edits keep the hash; a code edit changes it
+    assert bench.strip_comments(src.replace("trailing", "other words")) == out
+    assert bench.strip_comments(src.replace("int b;", "int b2;")) != out
