@@ -903,25 +903,33 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t col
 
 // CTAs that share one MMA tile in the launched kernels.
 constexpr int kCG = 2;
+constexpr int kMaxDevices = 64;
 
 template <int CG, bool FUSED, bool PROD>
-static int set_smem_attr() {
-    static cudaError_t err = cudaErrorUnknown;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes<CG, kUsesSlots<FUSED, PROD>>());
-    });
-    return err == cudaSuccess ? TGC_OK : cuda_fail(err);
+static int set_smem_attr(int dev) {
+    // a kernel's attributes belong to the device's context: set once per device
+    static std::mutex mu;
+    static cudaError_t err[kMaxDevices];
+    static bool done[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return TGC_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        err[dev] = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes<CG, kUsesSlots<FUSED, PROD>>());
+        done[dev] = true;
+    }
+    return err[dev] == cudaSuccess ? TGC_OK : cuda_fail(err[dev]);
 }
 
 // Persistent clusters that can be resident at once (one CTA per SM).
 template <int CG, bool FUSED, bool PROD>
-static int max_clusters(int sms) {
+static int max_clusters(int dev, int sms) {
     if (CG == 1) return sms;
-    static int cached = 0;
-    static std::once_flag once;
-    std::call_once(once, [sms] {
+    static std::mutex mu;
+    static int cached[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return sms / CG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -936,15 +944,18 @@ static int max_clusters(int sms) {
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED, PROD>, &cfg) != cudaSuccess || n <= 0)
             n = sms / CG;
-        cached = n;
-    });
-    return cached;
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
 
 template <int CG, bool FUSED, bool PROD>
 static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const GemmParams &p,
                   int nclusters, cudaStream_t stream) {
-    int rc = set_smem_attr<CG, FUSED, PROD>();
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_fail(de);
+    int rc = set_smem_attr<CG, FUSED, PROD>(dev);
     if (rc != TGC_OK) return rc;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
@@ -1076,11 +1087,11 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     // persistent clusters: every SM busy; for the plain GEMM no more clusters than tiles
     // (the shared-memory attribute must be set before the occupancy query)
     const int variant = !L.fused ? 0 : (L.producer ? 1 : 2);
-    int rc = variant == 0 ? set_smem_attr<kCG, false, false>()
-           : variant == 1 ? set_smem_attr<kCG, true, true>() : set_smem_attr<kCG, true, false>();
+    int rc = variant == 0 ? set_smem_attr<kCG, false, false>(dev)
+           : variant == 1 ? set_smem_attr<kCG, true, true>(dev) : set_smem_attr<kCG, true, false>(dev);
     if (rc != TGC_OK) return rc;
-    int nclusters = variant == 0 ? max_clusters<kCG, false, false>(sms)
-                  : variant == 1 ? max_clusters<kCG, true, true>(sms) : max_clusters<kCG, true, false>(sms);
+    int nclusters = variant == 0 ? max_clusters<kCG, false, false>(dev, sms)
+                  : variant == 1 ? max_clusters<kCG, true, true>(dev, sms) : max_clusters<kCG, true, false>(dev, sms);
     if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
     if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
     if (nclusters < 1) nclusters = 1;
