@@ -17,3 +17,10 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _library_built():
+    """libtgc.so is compiled in-tree (nvcc for sm_103a) if it is missing or older than its sources."""
+    from tile_gather_comm_gb300 import _build
+    _build.build()
