@@ -54,8 +54,10 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="large_skewed", choices=["large_skewed", "mlp_up", "square", "tiny"])
     p.add_argument("--quick", action="store_true", help="main line only: skip extras, e2e and cpu baseline")
-    p.add_argument("--only", choices=["all", "tgather"], default="all",
-                   help="tgather: time only the TGATHER workloads (small footprint, for profiling)")
+    p.add_argument("--only", choices=["all", "tgather", "gemm_vs_cublas"], default="all",
+                   help="tgather: time only the TGATHER workloads (small footprint, for profiling); "
+                        "gemm_vs_cublas: the plain GEMM and torch.matmul on the workload's gathered A, "
+                        "two warm-up calls each then one call each (for an ncu capture of both)")
     p.add_argument("--clock-ms", type=int, default=20, help="nvidia-smi sampling period")
     return p.parse_args(argv)
 
@@ -315,6 +317,8 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peaks_kind = load_peaks()
+    if args.only == "gemm_vs_cublas":
+        return gemm_vs_cublas(AG_CONFIGS[args.workload], dev, args)
     if args.only == "tgather":
         res = {"metric": METRIC, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
                "warmup": args.warmup, "note": "TGATHER only (profiling run)"}
@@ -435,6 +439,41 @@ def run_ours(args, dist: Dist):
     del shards, B, C, a
     torch.cuda.empty_cache()
     return res
+
+
+def gemm_vs_cublas(cfg, dev, args):
+    """The library's plain GEMM (MM_ONLY) and torch.matmul (cuBLAS) on the same gathered A and
+    B: two calls of each, then one of each, so that an ncu capture skipping the first four
+    launches sees one launch of each.  Prints their times for the record."""
+    import torch
+
+    import tile_gather_comm_gb300 as tgc
+    from tile_gather_comm_gb300.workloads import make_ag_inputs
+
+    sh, Bh = make_ag_inputs(cfg, seed=0)
+    shards = [x.to(dev) for x in sh]
+    B = Bh.to(dev)
+    C = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)
+    a = torch.cat(shards)
+    progress = torch.zeros(max(1, cfg.nblocks), dtype=torch.int32, device=dev)
+
+    def ours():
+        tgc.tgc_ag_matmul_ex(shards, B, C, a, cfg.cb, mode="mm_only", progress=progress, epoch=1)
+
+    def cublas():
+        torch.matmul(a, B.T, out=C)
+    ms = {}
+    for name, f in (("mm_only", ours), ("mm_only", ours), ("cublas", cublas), ("cublas", cublas),
+                    ("mm_only", ours), ("cublas", cublas)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1)
+    return {"metric": METRIC, "unit": "ms", "workload": cfg.name, "note": "plain GEMM vs cuBLAS, one call each "
+            "after two warm-up calls (profiling run)", "mm_only_ms": round(ms["mm_only"], 4),
+            "cublas_ms": round(ms["cublas"], 4)}
 
 
 def bench_other_workloads(dev, stream, dist, args, peaks):
