@@ -31,7 +31,7 @@
 //              shared-memory ring (128-byte swizzle)
 //   warp 1     TMEM owner; one lane (of the even CTA) issues tcgen05.mma into
 //              one of two TMEM accumulators (2 x 256 fp32 columns)
-//   warps 2, 3, 8..11  (FUSED) copy producer: 64 KiB pieces of comm blocks,
+//   warps 2, 3, 8..11  (FUSED) copy producer: 16-64 KiB pieces of comm blocks,
 //              handed out by a global ticket so any resident CTA can copy any
 //              block, moved with 16-byte register loads and stores (or, with
 //              TGC_COPY_LSU=0, by warp 2 alone with bulk async copies through
