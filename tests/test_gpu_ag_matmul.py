@@ -435,3 +435,33 @@ def test_random_shapes_against_oracle():
             run(mode=mode, pivot=pivot, rank=rank)
             assert torch.equal(run.C, ref), (i, R, H, cb, K, N, mode, pivot, rank)
             assert np.array_equal(bits16(run.a), a_ref), (i, mode)
+
+
+def test_soak_random_shapes_orders_modes_bit_exact():
+    """Many calls over random shapes, release orders, delays, tile orders, ranks, grids and both
+    fused producers: C bit-identical to the unfused path and `a` to the shards' concatenation,
+    with `a` NaN-filled before every call so that a read ahead of a block's flag shows up."""
+    g = torch.Generator().manual_seed(4242)
+    pick = lambda seq: seq[int(torch.randint(0, len(seq), (1,), generator=g))]
+    for shape_i in range(12):
+        R = pick([1, 2, 4, 8])
+        cb = pick([16, 64, 128, 256])
+        cfg, shards, B = _custom(R, cb * pick([1, 2, 4]), 8 * pick([8, 32, 64]), 8 * pick([32, 64, 96]), cb,
+                                 seed=500 + shape_i)
+        run = Run(cfg, shards, B)
+        run(mode="unfused")
+        ref = run.C.clone()
+        cat = torch.cat(run.shards)
+        for it in range(20):
+            mode = pick(["fused", "fused", "fused_ce"])
+            order = torch.randperm(cfg.nblocks, generator=g).tolist() if mode == "fused" else None
+            delay = (torch.randint(0, 3000, (cfg.nblocks,), generator=g).tolist()
+                     if mode == "fused" and it % 2 else None)
+            pivot = pick(["page", "shard", "none", "ready_queue"])
+            rank = int(torch.randint(0, R, (1,), generator=g))
+            grid = pick([0, 2, 16, 64])
+            run.a.view(torch.int16).fill_(-1)
+            run.C.zero_()
+            run(mode=mode, order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid)
+            assert torch.equal(run.C, ref), (shape_i, it, mode, pivot, rank, grid)
+            assert torch.equal(run.a, cat), (shape_i, it)
