@@ -608,7 +608,7 @@ def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_gpu / peaks["hbm_gbs"], 4),
                      "traffic": profiled_traffic(src_name, TGATHER_SOURCES),
-                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_flat_kernel<16>"},
+                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_flat_kernel<32>"},
     }
     del sets, g
     return out

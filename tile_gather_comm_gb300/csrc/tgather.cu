@@ -51,6 +51,9 @@ namespace tgc {
 #ifndef TGC_TG_CTAS_PER_SM
 #define TGC_TG_CTAS_PER_SM 8   // CTAs per SM in one wave
 #endif
+#ifndef TGC_TG_VW32
+#define TGC_TG_VW32 1          // flat kernel: 32-byte vectors when every address allows them
+#endif
 #ifndef TGC_TG_CHUNK
 #define TGC_TG_CHUNK 32768     // flat kernel: shares above this many bytes are cut into chunks
                                // dealt round-robin over the CTAs (0: one contiguous share each)
@@ -76,7 +79,10 @@ struct TGParams {
     uint32_t epoch;
 };
 
+struct alignas(32) Vec32 { uint32_t w[8]; };
+
 template <int VW> struct VecT;
+template <> struct VecT<32> { using T = Vec32; };
 template <> struct VecT<16> { using T = uint4; };
 template <> struct VecT<8> { using T = uint2; };
 template <> struct VecT<4> { using T = uint32_t; };
@@ -89,8 +95,24 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
+__device__ __forceinline__ Vec32 ld_stream(const Vec32 *p) {
+    Vec32 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                   "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
 template <typename T>
 __device__ __forceinline__ T ld_stream(const T *p) { return __ldg(p); }
+
+__device__ __forceinline__ void st_vec(Vec32 *p, const Vec32 &v) {
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void st_vec(T *p, const T &v) { *p = v; }
 
 // Element-wise copy of `n` bytes (n and both addresses multiples of es).
 __device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t n, int es, int tid, int nt) {
@@ -183,6 +205,7 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
 template <int VW>
 __global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams p, int64_t share, int64_t stride) {
     using V = typename VecT<VW>::T;
+    constexpr int U = VW == 32 ? kTGUnroll / 2 : kTGUnroll;  // the same bytes in flight per thread
 #if TGC_TG_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -209,17 +232,17 @@ __global__ void __launch_bounds__(kTGThreads) tgather_flat_kernel(const TGParams
             const int64_t body_end = head + nvec * VW;
             const V *vs = reinterpret_cast<const V *>(src + head);
             V *vd = reinterpret_cast<V *>(dst + head);
-            for (int64_t base = 0; base < nvec; base += (int64_t)kTGThreads * kTGUnroll) {
-                V reg[kTGUnroll];
+            for (int64_t base = 0; base < nvec; base += (int64_t)kTGThreads * U) {
+                V reg[U];
 #pragma unroll
-                for (int k = 0; k < kTGUnroll; ++k) {
+                for (int k = 0; k < U; ++k) {
                     const int64_t idx = base + tid + (int64_t)k * kTGThreads;
                     if (idx < nvec) reg[k] = ld_stream(vs + idx);
                 }
 #pragma unroll
-                for (int k = 0; k < kTGUnroll; ++k) {
+                for (int k = 0; k < U; ++k) {
                     const int64_t idx = base + tid + (int64_t)k * kTGThreads;
-                    if (idx < nvec) vd[idx] = reg[k];
+                    if (idx < nvec) st_vec(vd + idx, reg[k]);
                 }
             }
             if (head > 0) copy_elems(dst, src, head, p.es, tid, kTGThreads);
@@ -374,10 +397,10 @@ int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
 
-static int pick_vw(const TGatherLaunch &L) {
-    // Largest power of two <= 16 dividing every (src - dst) address difference;
+static int pick_vw(const TGatherLaunch &L, uint64_t widest = 16) {
+    // Largest power of two <= widest dividing every (src - dst) address difference;
     // then source and destination share their alignment modulo VW everywhere.
-    uint64_t g = 16;
+    uint64_t g = widest;
     const uint64_t slab_delta = (uint64_t)(L.dst_slab_bytes - L.run_bytes);
     auto fold = [&](uint64_t x) {
         while (g > 1 && (x % g) != 0) g >>= 1;
@@ -426,10 +449,11 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
         if (grid > slots) grid = slots;
         if (grid < 1) grid = 1;
         int64_t share = (total + grid - 1) / grid;
-        share = (share + 15) / 16 * 16;
+        const int vwf = TGC_TG_VW32 && vw == 16 ? pick_vw(L, 32) : vw;  // 32 only where 16 already holds
+        share = (share + 31) / 32 * 32;
         int64_t stride = 0;
         if (TGC_TG_CHUNK > 0 && share > TGC_TG_CHUNK) {
-            share = (TGC_TG_CHUNK + 15) / 16 * 16;
+            share = (TGC_TG_CHUNK + 31) / 32 * 32;
             stride = grid * share;
         }
         grid = (total + share - 1) / share;
@@ -443,7 +467,8 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = TGC_TG_PDL ? 1 : 0;
-        switch (vw) {
+        switch (vwf) {
+            case 32: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<32>, p, share, stride); break;
             case 16: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<16>, p, share, stride); break;
             case 8: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<8>, p, share, stride); break;
             case 4: e = cudaLaunchKernelEx(&cfg, tgather_flat_kernel<4>, p, share, stride); break;
