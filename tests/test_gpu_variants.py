@@ -4,7 +4,9 @@ library under the package's build folder and checked like the default build:
 - TGC_COPY_LSU=0: the fused kernel's producer is one warp of bulk async copies
   (global -> shared -> global through four slots) instead of register copies;
 - TGC_TG_CHUNK=0: the flat TGATHER kernel gives each CTA one contiguous share
-  instead of dealing 32 KiB chunks round-robin.
+  instead of dealing 32 KiB chunks round-robin;
+- TGC_TG_VW32=0: the flat TGATHER kernel moves 16-byte vectors where 32-byte
+  ones would do.
 
 Results must be identical to the oracle (TGATHER bit for bit, GEMM within the
 tolerance, bit for bit on integer-exact inputs) and to the default build's
@@ -26,7 +28,7 @@ from .test_gpu_ag_matmul import Run, _custom, _expected_pieces, _inputs, _oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0}
+VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0, "TGC_TG_VW32": 0}
 
 
 @pytest.fixture(scope="module")
