@@ -560,7 +560,7 @@ def bench_tgather_strided(tcfg, dev, dist, peaks, peaks_kind, pad: int = 64):
         "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<16>"},
+                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<32>"},
     }
     del sets, g
     return out

@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(256) tgather_strided_elems_kernel(const TGStri
 template <int VW>
 __global__ void __launch_bounds__(256) tgather_strided_rows_kernel(const TGStridedParams p, int64_t nseg) {
     using V = typename VecT<VW>::T;
-    constexpr int kSeg = 32 * kTGUnroll;  // vectors per segment
+    constexpr int U = VW == 32 ? kTGUnroll / 2 : kTGUnroll;  // the same bytes in flight per lane
+    constexpr int kSeg = 32 * U;                              // vectors per segment
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t items = p.rows * nseg;
@@ -316,16 +317,16 @@ __global__ void __launch_bounds__(256) tgather_strided_rows_kernel(const TGStrid
                                                  i * p.ss[3]);
         V *d = reinterpret_cast<V *>(p.dst + d0 * p.ds[0] + d1 * p.ds[1] + d2 * p.ds[2] +
                                      ((int64_t)r * p.H + i) * p.ds[3]);
-        V reg[kTGUnroll];
+        V reg[U];
 #pragma unroll
-        for (int j = 0; j < kTGUnroll; ++j) {
+        for (int j = 0; j < U; ++j) {
             const int64_t v = v0 + j * 32 + lane;
             if (v < p.nv) reg[j] = ld_stream(s + v);
         }
 #pragma unroll
-        for (int j = 0; j < kTGUnroll; ++j) {
+        for (int j = 0; j < U; ++j) {
             const int64_t v = v0 + j * 32 + lane;
-            if (v < p.nv) d[v] = reg[j];
+            if (v < p.nv) st_vec(d + v, reg[j]);
         }
     }
 }
@@ -350,7 +351,7 @@ int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64
     int vw = es;
     if (inner) {
         // widest vector every row start (source and destination) and the row length allow
-        uint64_t g = 16;
+        uint64_t g = TGC_TG_VW32 ? 32 : 16;
         auto fold = [&](uint64_t x) { while (g > (uint64_t)es && (x % g) != 0) g >>= 1; };
         for (int r = 0; r < nranks; ++r) fold(reinterpret_cast<uintptr_t>(srcs[r]));
         fold(reinterpret_cast<uintptr_t>(dst));
@@ -367,13 +368,14 @@ int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64
     if (e != cudaSuccess) return cuda_fail(e);
     const int64_t cap = (int64_t)sm_count(dev) * 8;
     if (inner) {
-        const int64_t seg = 32 * kTGUnroll;
+        const int64_t seg = 32 * (vw == 32 ? kTGUnroll / 2 : kTGUnroll);  // the kernel's kSeg
         const int64_t nseg = (p.nv + seg - 1) / seg;
         int64_t grid = (p.rows * nseg + 7) / 8;  // 8 warps per CTA, one item each per pass
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
         const dim3 gd((unsigned)grid), bd(256);
         switch (vw) {
+            case 32: tgather_strided_rows_kernel<32><<<gd, bd, 0, stream>>>(p, nseg); break;
             case 16: tgather_strided_rows_kernel<16><<<gd, bd, 0, stream>>>(p, nseg); break;
             case 8: tgather_strided_rows_kernel<8><<<gd, bd, 0, stream>>>(p, nseg); break;
             case 4: tgather_strided_rows_kernel<4><<<gd, bd, 0, stream>>>(p, nseg); break;
