@@ -428,6 +428,7 @@ def run_ours(args, dist: Dist):
         res["tgather_context_long"]["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the "
                                                "TGATHER workload; per-launch start and drain amortised")
         res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
+        res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
     res["clocks"] = sampler.stop(window=tuple(t_value))
 
     if not args.quick:
@@ -561,6 +562,60 @@ def bench_tgather_strided(tcfg, dev, dist, peaks, peaks_kind, pad: int = 64):
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<32>"},
+    }
+    del sets, g
+    return out
+
+
+def bench_tgather_release(tcfg, dev, dist, peaks, peaks_kind, chunk_rows: int = 128):
+    """tgc_tgather_ex with per-chunk progress release (chunks of `chunk_rows` rows, the
+    per-chunk counters and a gpu-scope release per chunk) on the TGATHER workload, graph-
+    replayed over rotating buffer sets > 4 x L2 like the plain TGATHER line."""
+    import torch
+
+    import tile_gather_comm_gb300 as tgc
+    from tile_gather_comm_gb300.workloads import make_tg_inputs
+
+    srcs_h = make_tg_inputs(tcfg, seed=0)
+    D0, D1, D2, H, W = tcfg.shape
+    per_set = tcfg.bytes_moved
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, -(-4 * l2 // per_set))
+    nchunks = tcfg.nranks * -(-H // chunk_rows)
+    sets = []
+    for _ in range(nsets):
+        srcs = [x.to(dev) for x in srcs_h]
+        dst = torch.empty((D0, D1, D2, tcfg.nranks * H, W), dtype=tcfg.dtype, device=dev)
+        progress = torch.zeros(nchunks, dtype=torch.int32, device=dev)
+        counters = torch.zeros(nchunks, dtype=torch.int32, device=dev)
+        sets.append((dst, srcs, progress, counters))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for dst, srcs, progress, counters in sets:
+            tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows, epoch=1,
+                               stream=s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for dst, srcs, progress, counters in sets:
+                tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows,
+                                   epoch=2, stream=s)
+    torch.cuda.synchronize()
+    reps = max(3, -(-400 // nsets))
+    ms = time_device(lambda: g.replay(), reps, 3, dist, torch.cuda.current_stream()) / nsets
+    gbs, _ = aggregate(ms, per_set, dist, scale=1e-9)
+    per_gpu = per_set / (ms * 1e-3) * 1e-9
+    released = all(bool(torch.all(x[2] == 2)) for x in sets)
+    out = {
+        "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(ms * 1e3, 3),
+        "config": f"{tcfg.nranks} x {str(tcfg.dtype).replace('torch.', '')} {tcfg.shape}, progress released per "
+                  f"{chunk_rows}-row chunk ({nchunks} flags)",
+        "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
+        "all_flags_released": released,
+        "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_kernel<16>"},
     }
     del sets, g
     return out

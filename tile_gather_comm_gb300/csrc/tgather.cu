@@ -174,10 +174,13 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
         }
 
         if (p.progress != nullptr) {
-            // Publish chunk (r, s) once all its nslab*tiles_per_seg items are written.
-            __threadfence();
+            // Publish chunk (r, s) once all its nslab*tiles_per_seg items are written.  The
+            // barrier orders every thread's stores of this item before thread 0, whose gpu-scope
+            // fence then makes them visible before the count; the other threads go on to their
+            // next item instead of each waiting for its own stores (measured +1.5-2%).
             __syncthreads();
             if (tid == 0) {
+                __threadfence();
                 const int64_t c = (int64_t)r * p.nseg + s;
                 const uint32_t target = (uint32_t)(p.nslab * p.tiles_per_seg);
                 const uint32_t old = atom_add_acq_rel_gpu(p.counters + c, 1u);
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
 }
 
 // Flat variant (no progress release): the work space is the concatenation of
-// all (slab, rank) runs, cut into gridDim.x equal, 16-byte-aligned shares --
+// all (slab, rank) runs, cut into gridDim.x equal, 32-byte-aligned shares --
 // every CTA of the one full wave moves the same number of bytes, so they
 // finish together.  A share larger than TGC_TG_CHUNK is dealt as chunks
 // instead: CTA c copies chunks c, c + gridDim.x, ..., so at any moment the
