@@ -6,7 +6,10 @@ library under the package's build folder and checked like the default build:
 - TGC_TG_CHUNK=0: the flat TGATHER kernel gives each CTA one contiguous share
   instead of dealing 32 KiB chunks round-robin;
 - TGC_TG_VW32=0: the flat TGATHER kernel moves 16-byte vectors where 32-byte
-  ones would do.
+  ones would do;
+- TGC_TMA_STORE_C=0: the GEMM epilogue stores C with per-thread 16-byte stores
+  instead of TMA stores of shared-memory boxes (the bulk-copy kernel always
+  does).
 
 Results must be identical to the oracle (TGATHER bit for bit, GEMM within the
 tolerance, bit for bit on integer-exact inputs) and to the default build's
@@ -28,7 +31,7 @@ from .test_gpu_ag_matmul import Run, _custom, _expected_pieces, _inputs, _oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0, "TGC_TG_VW32": 0}
+VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0, "TGC_TG_VW32": 0, "TGC_TMA_STORE_C": 0}
 
 
 @pytest.fixture(scope="module")

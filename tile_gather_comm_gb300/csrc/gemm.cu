@@ -85,6 +85,9 @@ namespace tgc {
 #ifndef TGC_COPY_HINT
 #define TGC_COPY_HINT 0          // producer's bulk loads of the shards and stores into `a`
 #endif
+#ifndef TGC_TMA_STORE_C
+#define TGC_TMA_STORE_C 1        // bf16 C leaves through shared memory and TMA stores
+#endif
 #ifndef TGC_A_HINT
 #define TGC_A_HINT 0             // tile loads of A
 #endif
@@ -126,10 +129,19 @@ struct Cfg {
 template <bool FUSED, bool PROD>
 constexpr bool kUsesSlots = FUSED && PROD && !TGC_COPY_LSU;
 
+// Epilogue staging for TMA stores of C: per epilogue warp, two buffers of 32
+// rows x 32 bf16 columns (64 bytes a row, 64-byte swizzle).  The bulk copy
+// producer's slots leave no room for it; that kernel stores C directly.
+constexpr int kCBoxCols = 32, kCBoxRows = 32;
+constexpr int kCBufBytes = kCBoxCols * kCBoxRows * 2;  // 2 KiB
+constexpr int kCStageBytes = 4 * 2 * kCBufBytes;       // 4 warps x 2 buffers
+template <bool SLOTS>
+constexpr bool kTmaC = TGC_TMA_STORE_C && !SLOTS;
+
 template <int CG, bool SLOTS>
 constexpr int smem_bytes() {
     return 1024 /* alignment slack */ + Cfg<CG, SLOTS>::kStages * (Cfg<CG, SLOTS>::kAStage + Cfg<CG, SLOTS>::kBStage) +
-           (SLOTS ? kSlots * kSlotBytes : 0) + 512 /* barriers + TMEM address */;
+           (SLOTS ? kSlots * kSlotBytes : 0) + (kTmaC<SLOTS> ? kCStageBytes : 0) + 512 /* barriers + TMEM address */;
 }
 
 static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<2, false>() <= 232448, "shared memory per CTA");
@@ -439,10 +451,21 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
     __syncwarp();
 }
 
+// 2-D tiled TMA store of a box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(map), "r"(smem_addr(smem_src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 template <int CG, bool FUSED, bool PROD>
-__device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *tempty, uint32_t tmem_base,
-                              uint32_t crank, int warp, int lane) {
+__device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8_t *sC, uint64_t *tfull,
+                              uint64_t *tempty, uint32_t tmem_base, uint32_t crank, int warp, int lane) {
     using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
+    constexpr bool kTma = kTmaC<kUsesSlots<FUSED, PROD>>;
+    const bool tma_c = kTma && !p.out_fp8;
+    uint8_t *stg = sC + (warp & 3) * 2 * kCBufBytes;  // this warp's two staging buffers
+    uint32_t stores = 0;                              // TMA stores this warp has issued
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     // the accumulator is released on the even CTA's barrier
@@ -494,6 +517,34 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
                 }
                 continue;
             }
+            if (kTma && tma_c) {
+                // Row `lane` of a 32 x 32 box goes to shared memory in the 64-byte swizzle
+                // (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)), then one lane stores
+                // the box with TMA; the tensor map clips rows >= M and columns >= N.
+                uint8_t *buf = stg + (stores & 1u) * kCBufBytes;
+                if (stores >= 2) {
+                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 o;
+                    o.x = pack_bf16x2(v[c * 8 + 0], v[c * 8 + 1]);
+                    o.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
+                    o.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
+                    o.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
+                    const int cs = c ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4 *>(buf + lane * 64 + cs * 16) = o;
+                }
+                fence_proxy_async_shared();  // the box is visible to the TMA unit
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmC, buf, n0 + j * 32, m - lane);
+                    bulk_commit();
+                }
+                ++stores;
+                continue;
+            }
             if (m < p.M) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -516,6 +567,8 @@ __device__ void role_epilogue(const GemmParams &p, uint64_t *tfull, uint64_t *te
             else mbar_arrive_cluster(tempty0 + acc * 8u);
         }
     }
+    if (kTma && lane == 0) bulk_wait<0>();  // every store of C has landed and read its buffer
+    __syncwarp();
     if (p.trace != nullptr && warp == 4 && lane == 0) {
         p.trace[blockIdx.x * kTraceWords + kTrEnd] = globaltimer_ns();
         p.trace[blockIdx.x * kTraceWords + kTrTiles] = tc;
@@ -786,7 +839,8 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
 template <int CG, bool FUSED, bool PROD>
 __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
-                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                   const GemmParams p) {
     using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -794,7 +848,8 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::kStages * C::kAStage;
     uint8_t *sSlot = sB + C::kStages * C::kBStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlot + (kUsesSlots<FUSED, PROD> ? kSlots * kSlotBytes : 0));
+    uint8_t *sC = sSlot + (kUsesSlots<FUSED, PROD> ? kSlots * kSlotBytes : 0);  // 2 KiB-aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + (kTmaC<kUsesSlots<FUSED, PROD>> ? kCStageBytes : 0));
     uint64_t *full = bars;
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
@@ -841,7 +896,7 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
             }
         }
     } else {
-        role_epilogue<CG, FUSED, PROD>(p, tfull, tempty, tmem_base, crank, warp, lane);
+        role_epilogue<CG, FUSED, PROD>(p, &tmC, sC, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
     // In a pair, the even CTA's MMAs read the odd CTA's shared memory and write
@@ -888,6 +943,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 row-major (rows x cols) with a (box_rows x 64) box, 128-byte swizzle.
+// C (rows x cols bf16, row-major) for TMA stores of 32 x 32 boxes, 64-byte swizzle.
+static bool make_map_c(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kCBoxCols, (cuuint32_t)kCBoxRows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows) {
     auto enc = encode_fn();
     if (enc == nullptr) return false;
@@ -950,7 +1019,8 @@ static int max_clusters(int dev, int sms) {
 }
 
 template <int CG, bool FUSED, bool PROD>
-static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const GemmParams &p,
+static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                  const GemmParams &p,
                   int nclusters, cudaStream_t stream) {
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
@@ -969,7 +1039,7 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD>, tmA, tmL, tmB, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD>, tmA, tmL, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
@@ -1039,9 +1109,11 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     const int sms = sm_count(dev);
 
-    CUtensorMap tmA, tmL, tmB;
+    CUtensorMap tmA, tmL, tmB, tmC;
     if (!make_map(&tmA, L.a, L.M, L.K, C::kRowsCta) || !make_map(&tmB, L.B, L.N, L.K, C::kHalfN))
         return TGC_ERR_CUDA;
+    // (for float8 output the epilogue stores C itself and this map is not used)
+    if (!make_map_c(&tmC, L.C, L.M, L.N)) return TGC_ERR_CUDA;
     if (L.fused) {
         if (!make_map(&tmL, L.shards[L.rank], rows_per_rank, L.K, C::kRowsCta)) return TGC_ERR_CUDA;
         p.cb = (int)L.cb;
@@ -1102,9 +1174,9 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.piece_bytes = kMaxPieceBytes;
     }
     if (L.fused) p.pieces_per_block = (int)((p.block_bytes + p.piece_bytes - 1) / p.piece_bytes);
-    return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, p, nclusters, stream)
-         : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, p, nclusters, stream)
-                        : launch<kCG, true, false>(tmA, tmL, tmB, p, nclusters, stream);
+    return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, tmC, p, nclusters, stream)
+         : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, tmC, p, nclusters, stream)
+                        : launch<kCG, true, false>(tmA, tmL, tmB, tmC, p, nclusters, stream);
 }
 
 }  // namespace tgc
