@@ -28,7 +28,6 @@ import datetime
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -59,6 +58,11 @@ def parse_args(argv=None):
                         "gemm_vs_cublas: the plain GEMM and torch.matmul on the workload's gathered A, "
                         "two warm-up calls each then one call each (for an ncu capture of both)")
     p.add_argument("--clock-ms", type=int, default=20, help="nvidia-smi sampling period")
+    p.add_argument("--pivot", default="auto", choices=["auto", "page", "shard", "none", "ready_queue"],
+                   help="tile order of the headline call (auto: the library's choice, as tgc_ag_matmul)")
+    p.add_argument("--band-n", type=int, default=0,
+                   help="tile raster of the headline call: 0 = the library's choice, > 0 = bands of that many "
+                        "tile columns, < 0 = the group raster")
     return p.parse_args(argv)
 
 
@@ -151,18 +155,21 @@ def sources_sha(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(summary_name: str, sources, per_launch_units: float | None = None):
-    """DRAM bytes per launch recorded in a profiles/ summary, if taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", summary_name)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def profiled_traffic(key: str, sources):
+    """DRAM bytes (read + write) per launch of one kernel on one workload, as an ncu capture
+    recorded them in profiles/traffic.json, if the capture was taken on the current kernel
+    sources (same comment-stripped hash); otherwise None."""
     try:
-        text = open(path, encoding="utf-8").read()
-    except OSError:
+        with open(TRAFFIC_FILE, encoding="utf-8") as f:
+            entry = json.load(f).get(key)
+    except (OSError, ValueError):
         return None
-    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
-    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != sources_sha(sources):
+    if not entry or entry.get("source_sha256_16") != sources_sha(sources):
         return None
-    return float(m_b.group(1))
+    return float(entry["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -192,7 +199,9 @@ class ClockSampler:
 
     def stop(self, window: tuple | None = None):
         """Summary of the samples.  `window` = (t0, t1) in time.time() seconds: the
-        region whose clocks `sm_mhz` reports (all samples under load if none fell in it)."""
+        region whose clocks `sm_mhz` reports (all samples under load if none fell in it).
+        The raw lines stay in `self.lines` for summaries of other windows."""
+        self.lines = []
         if self.proc is None:
             return None
         time.sleep(0.2)
@@ -202,9 +211,9 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         with open(self.path) as f:
-            lines = f.readlines()
+            self.lines = f.readlines()
         os.unlink(self.path)
-        return clock_summary(lines, window)
+        return clock_summary(self.lines, window)
 
 
 def clock_summary(lines, window: tuple | None = None):
@@ -326,6 +335,7 @@ def run_ours(args, dist: Dist):
         res["value"] = res["tgather"]["value"]
         res["tgather_ragged_i32"] = bench_tgather(TG_CONFIGS["ragged_i32"], dev, stream, dist, peaks,
                                                   peaks_kind, args)
+        res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         return res
     cfg = AG_CONFIGS[args.workload]
     flops = float(cfg.flops)
@@ -345,12 +355,12 @@ def run_ours(args, dist: Dist):
     epoch = [0]
     launches = [0]
 
-    def call(mode="fused", delays=True, pivot="page", out=None, out_format="bf16"):
+    def call(mode="fused", delays=True, pivot=args.pivot, out=None, out_format="bf16", band_n=args.band_n):
         epoch[0] += 1
         tgc.tgc_ag_matmul_ex(shards, B, C if out is None else out, a, cfg.cb, mode=mode, progress=progress,
                              epoch=epoch[0], workspace=ws, order=order if mode == "fused" else None,
                              delay_ns=delay if (mode == "fused" and delays) else None, stream=stream,
-                             pivot=pivot, out_format=out_format)
+                             pivot=pivot, out_format=out_format, band_n=band_n)
         launches[0] += 2 if mode == "unfused" else 1
 
     sampler = ClockSampler(dist.local_rank, args.clock_ms)
@@ -373,14 +383,15 @@ def run_ours(args, dist: Dist):
                         f"B bf16 ({cfg.N},{cfg.K}) ~N(0,{cfg.b_sigma}), comm_block_rows={cfg.cb}"
                         + (", seeded release permutation + delays U[0,20us]" if cfg.skewed else ""),
             "M": cfg.M, "N": cfg.N, "K": cfg.K, "R": cfg.R, "comm_block_rows": cfg.cb, "rank": 0,
-            "pivot": "page", "parallelism": f"replicas x{dist.world} (the path does not shard)",
+            "pivot": args.pivot, "band_n": args.band_n,
+            "parallelism": f"replicas x{dist.world} (the path does not shard)",
             "l2": "inputs larger than L2 (shards 4x128 MiB + B 128 MiB); no flush",
             "timing": "CUDA events on the launching stream around exactly `steps` calls, max over ranks",
         },
         "gpu_launches": fused_launches_timed,
         "step_ms_percentiles": percentiles(step_ms),
     }
-    prof = profiled_traffic("ag_gemm_fused_large_skewed.md", KERNEL_SOURCES) if cfg.name == "large_skewed" else None
+    prof = profiled_traffic(f"ag_gemm_fused/{cfg.name}", KERNEL_SOURCES)
     res["roofline"] = {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peaks["bf16_tflops"],
                        "unit": "TFLOP/s", "frac": round(kernel_tflops / peaks["bf16_tflops"], 4),
                        "traffic": prof, "peak_source": f"{peaks_kind} burst cuBLAS bf16",
@@ -397,6 +408,7 @@ def run_ours(args, dist: Dist):
         variants = {"fused": lambda: call("fused"), "unfused": lambda: call("unfused"),
                     "mm_only": lambda: call("mm_only"),
                     "ready_queue": lambda: call("fused", pivot="ready_queue"),
+                    "page_group": lambda: call("fused", pivot="page", band_n=-1),
                     "fused_ce": lambda: call("fused_ce"),
                     "fused_fp8_out": lambda: call("fused", out=C8, out_format="f8e4m3"),
                     "cublas_gemm": cublas}
@@ -410,6 +422,7 @@ def run_ours(args, dist: Dist):
         res["unfused"]["kernels_per_step"] = 2
         res["mm_only"]["frac_of_peak"] = round(flops / (med["mm_only"] * 1e-3) * 1e-12 / peaks["bf16_tflops"], 4)
         res["ready_queue"]["note"] = "same workload, READY_QUEUE tile order"
+        res["page_group"]["note"] = "same workload, the page's rank pivot on the group raster (GROUP_SIZE_M swizzle)"
         res["cublas_gemm"]["note"] = ("context: torch.matmul (cuBLAS) on the already gathered A, "
                                       "same shapes; not part of this library")
         res["fused_ce"]["note"] = ("same workload, copy-engine producer: cudaMemcpyAsync per block on library "
@@ -429,7 +442,28 @@ def run_ours(args, dist: Dist):
                                                "TGATHER workload; per-launch start and drain amortised")
         res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
+        # the same fused call over a region of at least a second: the GPU settles at its power
+        # cap, so this is the figure to set against the sustained cuBLAS peak
+        n_sus = max(args.steps, int(1.2e3 / max(ms_fused, 1e-3)) + 1)
+        t_sus = [0.0, 0.0]
+        ms_sus = time_device(lambda: call("fused"), n_sus, 3, dist, stream, wall=t_sus)
+        v_sus, ms_sus_max = aggregate(ms_sus, flops, dist)
+        k_sus = flops / (ms_sus * 1e-3) * 1e-12
+        res["sustained"] = {
+            "value": round(v_sus, 2), "unit": "TFLOP/s", "steps": n_sus, "ms_per_step": round(ms_sus_max, 4),
+            "region_s": round(t_sus[1] - t_sus[0], 3),
+            "frac_of_sustained_peak": round(k_sus / peaks["bf16_tflops_sustained"], 4),
+            "frac_of_burst_peak": round(k_sus / peaks["bf16_tflops"], 4),
+            "sustained_peak": peaks["bf16_tflops_sustained"],
+            "peak_source": f"{peaks_kind} cuBLAS bf16 held for seconds under the power cap",
+            "note": "the headline step (same call) timed over >= 1.2 s; `value` above is its first "
+                    f"{args.steps} steps after {args.warmup} warm-up calls"}
     res["clocks"] = sampler.stop(window=tuple(t_value))
+    if "sustained" in res and sampler.lines:
+        cs = clock_summary(sampler.lines, tuple(t_sus))
+        if cs is not None:
+            res["sustained"]["clocks"] = {"sm_mhz": cs["sm_mhz"], "samples": cs["samples_in_value_region"],
+                                          "reasons": cs["reasons"]}
 
     if not args.quick:
         res["other_workloads"] = bench_other_workloads(dev, stream, dist, args, peaks)
@@ -503,12 +537,16 @@ def bench_other_workloads(dev, stream, dist, args, peaks):
             ep[0] += 1
             tgc.tgc_ag_matmul_ex(shards, B, C, a, cfg.cb, mode=mode, pivot=pivot, progress=progress,
                                  epoch=ep[0], workspace=ws, stream=stream)
-        med = time_interleaved({"fused": lambda: call("fused"),
+        med = time_interleaved({"fused": lambda: call("fused", "auto"),
+                                "fused_page": lambda: call("fused", "page"),
                                 "fused_ready_queue": lambda: call("fused", "ready_queue"),
                                 "unfused": lambda: call("unfused"), "mm_only": lambda: call("mm_only")},
                                max(args.steps, 300), dist, stream, rounds=10)
         line = {k: round(aggregate(v, float(cfg.flops), dist)[0], 1) for k, v in med.items()}
         line["unit"] = "TFLOP/s"
+        line["fused_is"] = "the default call: tile order TGC_PIVOT_AUTO (as tgc_ag_matmul)"
+        line["fused_over_unfused"] = round(med["unfused"] / med["fused"], 4)
+        line["fused_page_over_unfused"] = round(med["unfused"] / med["fused_page"], 4)
         line["fused_ready_queue_over_unfused"] = round(med["unfused"] / med["fused_ready_queue"], 4)
         line["config"] = f"{cfg.R} x ({cfg.H},{cfg.K}) shards, B ({cfg.N},{cfg.K}), cb={cfg.cb}"
         out[name] = line
@@ -614,7 +652,8 @@ def bench_tgather_release(tcfg, dev, dist, peaks, peaks_kind, chunk_rows: int = 
         "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
         "all_flags_released": released,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(per_gpu / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(f"tgather_release/{tcfg.name}", TGATHER_SOURCES),
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_kernel<16>"},
     }
     del sets, g
@@ -655,14 +694,14 @@ def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
     ms = ms_graph / nsets
     gbs, _ = aggregate(ms, per_set, dist, scale=1e-9)
     per_gpu = per_set / (ms * 1e-3) * 1e-9
-    src_name = {"bw_f16": "tgather_bw_f16.md", "ragged_i32": "tgather_ragged_i32.md"}.get(tcfg.name, "")
+
     out = {
         "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(ms * 1e3, 3),
         "config": f"{tcfg.nranks} x {str(tcfg.dtype).replace('torch.', '')} {tcfg.shape} -> dst DIM_3 x{tcfg.nranks}",
         "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_gpu / peaks["hbm_gbs"], 4),
-                     "traffic": profiled_traffic(src_name, TGATHER_SOURCES),
+                     "traffic": profiled_traffic(f"tgather_flat/{tcfg.name}", TGATHER_SOURCES),
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_flat_kernel<32>"},
     }
     del sets, g

@@ -44,7 +44,10 @@ typedef enum tgc_status {
     TGC_ERR_INVALID_ARG = -1,  /* null pointer, bad count or shape, bad mode   */
     TGC_ERR_DTYPE = -2,        /* unknown dtype                               */
     TGC_ERR_ALIGN = -3,        /* pointer or row pitch misaligned for the path */
-    TGC_ERR_NOT_RESIDENT = -4, /* the persistent grid cannot be made resident */
+    /* -4 is not used: the persistent grids are sized from the occupancy the
+       device reports, and no kernel needs more of its CTAs resident at once
+       than that (copy work is handed out by tickets), so a grid that cannot
+       launch is a launch error (TGC_ERR_CUDA). */
     TGC_ERR_CUDA = -5,         /* a CUDA call failed: see tgc_last_cuda_error */
     TGC_ERR_TIMEOUT = -6,      /* a bounded device wait expired               */
     TGC_ERR_ABORTED = -7,      /* the kernel stopped because another CTA timed out */
@@ -158,7 +161,8 @@ int tgc_tgather_ex(const tgc_tgather_args *args);
  * with the gather cut into communication blocks of comm_block_rows rows, each
  * published through a progress flag, and the MatMul tiles consuming each
  * block as soon as its flag is set ([AGM] sections 融合后的流水线 and
- * MatMul 按需等待远端分片).  The result equals gather-then-MatMul.
+ * MatMul 按需等待远端分片).  The result equals gather-then-MatMul.  Runs as
+ * tgc_ag_matmul_ex with mode FUSED, rank 0, tile order TGC_PIVOT_AUTO.
  *
  * a_shards        host array of nranks device pointers, each (M/nranks, K)
  *                 bf16, 16-byte aligned.
@@ -169,13 +173,17 @@ int tgc_tgather_ex(const tgc_tgather_args *args);
  * TMA), K > 0.
  * Temporaries (`a`, progress flags, workspace) are allocated stream-ordered
  * from a memory pool the library creates per device (cudaMallocFromPoolAsync)
- * and freed the same way; the pool keeps freed memory for the next call.  This entry point synchronizes
- * `stream` before returning so that it can report a device-side error.
+ * and freed the same way.  The pool keeps up to TGC_POOL_KEEP_BYTES of freed
+ * memory mapped for the next call and returns the rest to the device when
+ * the stream synchronizes, so a large call does not pin its `a` (M*K*2 bytes)
+ * for the life of the process.  This entry point synchronizes `stream` before
+ * returning so that it can report a device-side error.
  * M == 0 or N == 0: returns TGC_OK, nothing written.
  */
 int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *C,
                   int64_t M, int64_t K, int64_t N, int64_t comm_block_rows,
                   cudaStream_t stream);
+#define TGC_POOL_KEEP_BYTES ((uint64_t)256 << 20)
 
 typedef enum tgc_mode {
     TGC_MODE_FUSED = 0,    /* one kernel: copy blocks into a_out + flag-waiting GEMM */
@@ -188,7 +196,14 @@ typedef enum tgc_mode {
                               数据搬运与细粒度同步: the backend stream copies every
                               (src_rank, split_id) chunk and then stream_write_value32's
                               its progress entry).  delay_ns is ignored and READY_QUEUE
-                              behaves as PAGE in this mode. */
+                              behaves as PAGE in this mode.  This mode relies on the
+                              device-to-device cudaMemcpyAsync running on the GPU's
+                              copy engines while the persistent GEMM kernel holds
+                              every SM: should the runtime ever carry such a copy out
+                              with a kernel of its own, that kernel could not start
+                              before the GEMM ends, the GEMM's flag waits would expire
+                              and the call would return TGC_ERR_TIMEOUT (after
+                              spin_timeout_ns) instead of a result. */
 } tgc_mode;
 
 /*
@@ -214,7 +229,14 @@ typedef enum tgc_pivot {
     TGC_PIVOT_PAGE = 0,
     TGC_PIVOT_SHARD = 1,
     TGC_PIVOT_NONE = 2,
-    TGC_PIVOT_READY_QUEUE = 3
+    TGC_PIVOT_READY_QUEUE = 3,
+    TGC_PIVOT_AUTO = 4  /* the library's choice.  FUSED: READY_QUEUE when the caller passes
+                           a release `order` and the band raster is in use (blocks then
+                           arrive out of tile order while rows are walked one at a time),
+                           PAGE otherwise (with the default release order the two orders
+                           coincide).  FUSED_CE: PAGE.  UNFUSED and MM_ONLY: NONE (no tile
+                           waits there).  The order tgc_ag_matmul and
+                           tgc_ag_matmul_noalloc use. */
 } tgc_pivot;
 
 /* Element type of C.  F8E4M3: float8 e4m3 ("fn": bias 7, no infinities,
@@ -252,7 +274,18 @@ typedef enum tgc_out_format {
  *                %globaltimer before it publishes the block (injected arrival
  *                skew).
  *   spin_timeout_ns  limit for every device wait; 0 = 2 s.
- *   group_m      tile rows per swizzle group; 0 = default (8).
+ *   group_m      tile rows per swizzle group of the group raster; 0 = default (8).
+ *   band_n       tile raster.  > 0: band raster -- the tiles are taken in bands
+ *                of band_n tile columns, each band walking the tile rows in
+ *                order (the rank rotation still applies to the rows), which
+ *                keeps the band's columns of B in L2 and asks for the rows of
+ *                `a` in the order the producer publishes them; < 0: group
+ *                raster (group_m tile rows per group, column-major inside a
+ *                group: the page's GROUP_SIZE_M swizzle); 0: the library's
+ *                choice -- for FUSED and FUSED_CE, bands of TGC_DEFAULT_BAND_N
+ *                columns when one shard holds fewer whole tile rows (256 rows
+ *                each) than group_m, else the group raster; the group raster
+ *                for UNFUSED and MM_ONLY.
  *   grid         persistent CTAs (used in pairs); 0 = every SM.
  *   workspace    device memory of tgc_ag_matmul_workspace_bytes() bytes,
  *                128-byte aligned, zero-filled once by the caller before first
@@ -265,12 +298,18 @@ typedef enum tgc_out_format {
  *                not kept (UNFUSED / MM_ONLY without workspace).
  *   sync         nonzero: synchronize `stream` and return the device status.
  *   out_format   element type of C (tgc_out_format; 0 = bf16).
- *   trace        optional device uint64 array of grid*TGC_TRACE_WORDS words
- *                (grid = the persistent CTA count actually launched, at most
- *                the SM count): per CTA, %globaltimer stamps and signal-wait
- *                totals, laid out as the TGC_TRACE_* indices below.  NULL
- *                records nothing.  The page's evaluation advice asks for the
- *                time spent waiting on signals to be reported separately.
+ *   trace        optional device uint64 array of trace_words words: per
+ *                launched CTA, TGC_TRACE_WORDS words of %globaltimer stamps
+ *                and signal-wait totals, laid out as the TGC_TRACE_* indices
+ *                below (CTA i at word i*TGC_TRACE_WORDS).  NULL records
+ *                nothing.  The page's evaluation advice asks for the time
+ *                spent waiting on signals to be reported separately.
+ *   trace_words  words of `trace`.  The kernels launch CTAs in pairs, at
+ *                most one per SM, and no more than max(grid, 2) when grid is
+ *                nonzero, so with a trace this must be at least
+ *                TGC_TRACE_WORDS * min(max(grid, 2), SM count of the current
+ *                device) -- the SM count when grid is 0; a smaller value is
+ *                TGC_ERR_INVALID_ARG.
  * Calls that share a workspace or progress array must not overlap on the GPU.
  */
 typedef struct tgc_ag_matmul_args {
@@ -299,9 +338,13 @@ typedef struct tgc_ag_matmul_args {
     cudaStream_t stream;
     uint64_t *trace;
     tgc_out_format out_format;
+    size_t trace_words;
+    int band_n;
 } tgc_ag_matmul_args;
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
+
+#define TGC_DEFAULT_BAND_N 16
 
 /* Per-CTA trace words (times in ns of %globaltimer). */
 #define TGC_TRACE_WORDS 16
@@ -331,13 +374,20 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
  * Arguments as in tgc_ag_matmul, plus
  *   a_out   device (M, K) bf16 output: the gathered A (as in tgc_ag_matmul_ex).
  * The scratch the fused kernel needs (status word, ticket dispenser, per-block
- * counters and progress flags) lives in a fixed 64 KiB array of device memory
- * declared statically in the library, one per GPU that loads the library and
- * held until the process exits.  Limit: M / comm_block_rows <= 
- * TGC_NOALLOC_MAX_BLOCKS comm blocks; larger problems return
- * TGC_ERR_TOO_LARGE before anything is enqueued.
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * counters and progress flags, per-tile-row counters and ready ring) lives in
+ * a fixed array of TGC_NOALLOC_SCRATCH_BYTES of device memory declared
+ * statically in the library, one per GPU that loads the library and held
+ * until the process exits.  Limits, both checked before anything is
+ * enqueued, TGC_ERR_TOO_LARGE otherwise:
+ *   - M / comm_block_rows <= TGC_NOALLOC_MAX_BLOCKS comm blocks;
+ *   - the scratch bytes fit the array: 16 bytes per comm block (counter,
+ *     flag, two host-array copies) plus 12 bytes per 256-row tile row of M
+ *     plus a few hundred bytes of fixed fields, each region rounded up to
+ *     128 bytes.  With 2048 blocks this caps M at about 700,000 rows.
+ * Each call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, which allocates nothing), so the address stays
+ * right after a device reset; make the first call on a device before any
+ * stream capture, since that lookup may load the library's module.
  * Every call on a device shares the same array, which keeps the previous
  * call's contents: each call clears the part it uses (cudaMemsetAsync on
  * `stream`) before launching.  Calls that overlap on the GPU -- on different
@@ -346,6 +396,7 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
  * Synchronizes `stream` and returns the device status, like tgc_ag_matmul.
  */
 #define TGC_NOALLOC_MAX_BLOCKS 2048
+#define TGC_NOALLOC_SCRATCH_BYTES 65536
 int tgc_ag_matmul_noalloc(const void *const *a_shards, int nranks, const void *B, void *C, void *a_out,
                           int64_t M, int64_t K, int64_t N, int64_t comm_block_rows,
                           cudaStream_t stream);
@@ -359,13 +410,16 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
  * device uses).  A tile is tgc_gemm_tile_shape()'s BM x BN outputs, computed
  * by one persistent cluster (a pair of CTAs on two SMs).  Writes, for cluster
  * `cta` of `grid` persistent clusters, the sequence of (pid_m, pid_n) pairs it
- * processes into out[2*t], out[2*t+1], at most max_tiles pairs; returns the
+ * processes (band_n > 0: band raster of band_n tile columns; band_n <= 0:
+ * group raster of group_m tile rows, 0 = 8) into out[2*t], out[2*t+1], at
+ * most max_tiles pairs; returns the
  * number of tiles of that cluster, or a negative tgc_status.  Needs no GPU.
- * READY_QUEUE has no static order past its local prefix: TGC_ERR_INVALID_ARG.
+ * READY_QUEUE has no static order past its local prefix, and AUTO may choose
+ * it: both are TGC_ERR_INVALID_ARG here.
  */
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks,
-                               int rank, tgc_pivot pivot, int group_m, int grid, int cta,
-                               int64_t *out, int64_t max_tiles);
+                               int rank, tgc_pivot pivot, int group_m, int band_n, int grid,
+                               int cta, int64_t *out, int64_t max_tiles);
 
 /* Tile shape used by the GEMM kernels (BM, BN, BK): BM rows are shared by a
  * pair of CTAs (128 each), BK is the K depth of one pipeline stage. */

@@ -27,3 +27,10 @@ def requires_gpu():
     import pytest
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
+
+
+def trace_buffer(words_per_cta: int) -> torch.Tensor:
+    """Zeroed device buffer for the per-CTA trace: one record per SM of the current device
+    (the kernels launch at most one CTA per SM)."""
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return torch.zeros(nsm * words_per_cta, dtype=torch.int64, device="cuda")

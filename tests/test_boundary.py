@@ -131,6 +131,22 @@ def test_ag_matmul_invalid_arguments():
     assert _lib.lib().tgc_ag_matmul_ex(None) == E.TGC_ERR_INVALID_ARG
     assert _ag(out_format=1, N=72) == E.TGC_ERR_ALIGN       # fp8 C needs N % 16 == 0
     assert _ag(out_format=5) == E.TGC_ERR_INVALID_ARG
+    # a trace must hold at least one CTA pair's records (the SM-count bound is checked on a GPU)
+    assert _ag(trace=FAKE, trace_words=0) == E.TGC_ERR_INVALID_ARG
+    assert _ag(trace=FAKE, trace_words=2 * E.TRACE_WORDS - 1) == E.TGC_ERR_INVALID_ARG
+    assert _ag(trace=FAKE + 4, trace_words=1 << 16) == E.TGC_ERR_ALIGN
+
+
+def test_status_codes_match_header_and_unused_code_is_unknown():
+    """Every status the header declares has its own string; -4 (once "not resident") is unused:
+    the persistent grids are sized from the device's reported occupancy, so no path returns it."""
+    hdr = open(HEADER, encoding="utf-8").read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(TGC_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", hdr)}
+    assert "TGC_ERR_NOT_RESIDENT" not in codes and -4 not in codes.values()
+    for name, code in codes.items():
+        assert getattr(_lib, name) == code, name
+        assert tgc.tgc_status_string(code) != "unknown status", name
+    assert tgc.tgc_status_string(-4) == "unknown status"
 
 
 def test_ag_matmul_empty_problem_is_ok():
@@ -157,19 +173,21 @@ def test_workspace_bytes_grows_with_blocks():
 # ----------------------------------------------------------------------------- schedule
 
 
-def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0):
-    seqs = [tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, pivot, group_m, grid, c) for c in range(grid)]
+def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0, band_n=0):
+    seqs = [tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, pivot, group_m, grid, c, band_n=band_n)
+            for c in range(grid)]
     return seqs
 
 
 @pytest.mark.parametrize("M,N,cb,R", [(4096, 4096, 128, 8), (8192, 14336, 256, 8), (32768, 8192, 512, 4),
                                       (64, 64, 8, 4), (1000 * 8, 1000, 1000, 8)])
 @pytest.mark.parametrize("pivot", ["page", "shard", "none"])
-def test_schedule_is_a_permutation(M, N, cb, R, pivot):
+@pytest.mark.parametrize("band_n", [0, 16, 3])
+def test_schedule_is_a_permutation(M, N, cb, R, pivot, band_n):
     bm, bn, _ = tgc.tgc_gemm_tile_shape()
     npm, npn = -(-M // bm), -(-N // bn)
     for rank in sorted({0, 1, R - 1}):
-        seqs = _all_tiles(M, N, cb, R, rank, pivot, grid=148)
+        seqs = _all_tiles(M, N, cb, R, rank, pivot, grid=148, band_n=band_n)
         tiles = [t for s in seqs for t in s]
         assert len(tiles) == npm * npn
         assert len(set(tiles)) == npm * npn
@@ -197,6 +215,24 @@ def test_page_pivot_matches_formula_and_starts_on_local_shard_when_one_block_per
         assert seq[0][0] * bm // (M // R) == rank
 
 
+@pytest.mark.parametrize("M,N,cb,R,band_n", [(8192, 14336, 256, 8, 16), (32768, 8192, 512, 4, 16),
+                                             (4096, 4096, 128, 8, 5), (1000 * 8, 1000, 1000, 8, 2)])
+def test_band_raster_walks_rows_in_order_within_each_band(M, N, cb, R, band_n):
+    """Band raster: tiles in bands of band_n tile columns, row-major inside a band, the rank
+    rotation applied to the rows after it; with the page pivot, rank r's walk starts on the row
+    the page's formula gives and every band visits the rows in that rotated order."""
+    bm, bn, _ = tgc.tgc_gemm_tile_shape()
+    npm, npn = -(-M // bm), -(-N // bn)
+    for rank in sorted({0, R - 1}):
+        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", 8, 1, 0, band_n=band_n)
+        assert len(seq) == npm * npn
+        off = (rank * cb // bm) % npm
+        for t, (pm, pn) in enumerate(seq):
+            band, r = divmod(t, band_n * npm)
+            bw = min(npn - band * band_n, band_n)
+            assert (pm, pn) == ((r // bw + off) % npm, band * band_n + r % bw)
+
+
 def test_shard_pivot_starts_every_rank_on_its_shard():
     M, N, cb, R = 8192, 14336, 256, 8
     bm = tgc.tgc_gemm_tile_shape()[0]
@@ -206,6 +242,9 @@ def test_shard_pivot_starts_every_rank_on_its_shard():
 
 
 def test_schedule_rejects_bad_arguments():
+    for dynamic in ("ready_queue", "auto"):  # no static order past the local prefix
+        with pytest.raises(tgc.TGCError):
+            tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 0, dynamic, 8, 1, 0)
     with pytest.raises(tgc.TGCError):
         tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 4, "page", 8, 1, 0)
     with pytest.raises(tgc.TGCError):

@@ -19,7 +19,7 @@ from tile_gather_comm_gb300 import _lib
 from tile_gather_comm_gb300.workloads import (AG_CONFIGS, AGConfig, make_ag_inputs, make_release_schedule,
                                               sample_rows)
 
-from .helpers import assert_within_tol, bits16, requires_gpu
+from .helpers import assert_within_tol, bits16, requires_gpu, trace_buffer
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -82,7 +82,7 @@ def _custom(R, H, K, N, cb, seed=0, sigma=1.0):
 
 
 @pytest.mark.parametrize("mode", ["fused", "unfused", "fused_ce"])
-@pytest.mark.parametrize("pivot", ["page", "shard", "none", "ready_queue"])
+@pytest.mark.parametrize("pivot", ["page", "shard", "none", "ready_queue", "auto"])
 def test_tiny_all_ranks(mode, pivot):
     cfg, shards, B = _inputs("tiny")
     C_ref, a_ref = _oracle_full(shards, B)
@@ -106,10 +106,11 @@ def test_ragged_shapes_full(R, H, K, N, cb):
     run = Run(cfg, shards, B)
     for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue"), ("fused_ce", "page")):
         for rank in sorted({0, R - 1}):
-            run.C.zero_()
-            run(mode=mode, rank=rank, pivot=pivot)
-            assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank}")
-            assert np.array_equal(bits16(run.a), a_ref)
+            for band_n in (0, -1, 1):  # default (bands for the fused modes), group raster, one-column bands
+                run.C.zero_()
+                run(mode=mode, rank=rank, pivot=pivot, band_n=band_n)
+                assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank} band {band_n}")
+                assert np.array_equal(bits16(run.a), a_ref)
 
 
 @pytest.mark.parametrize("R,H,K,N", [(4, 16, 64, 64), (2, 128, 64, 512), (4, 96, 128, 248)])
@@ -217,7 +218,9 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     run(mode="fused", **kw)
     C_fused = run.C.clone()
     assert torch.equal(run.a, torch.cat(run.shards))
-    rows = sample_rows(cfg, seed=0, per_block_random=2 if cfg.M <= 8192 else 0)
+    # the first and last row of every comm block plus two seeded interior rows of each, so
+    # that interior TMEM lanes of both CTAs of a pair are compared with the oracle too
+    rows = sample_rows(cfg, seed=0, per_block_random=2)
     ref = oracle.ag_matmul_rows([bits16(s) for s in shards], bits16(B), rows)
     assert_within_tol(C_fused[rows], ref, name)
     run.C.zero_()
@@ -275,7 +278,7 @@ def test_explicit_grid_sizes_give_identical_results():
 def test_trace_records_every_cta():
     cfg, shards, B = _custom(4, 512, 256, 1024, 64, seed=12)
     run = Run(cfg, shards, B)
-    trace = torch.zeros(152 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+    trace = trace_buffer(_lib.TRACE_WORDS)
     run(trace=trace)
     t = trace.view(-1, _lib.TRACE_WORDS).cpu()
     used = t[t[:, _lib.TRACE["start"]] > 0]
@@ -299,7 +302,7 @@ def test_copy_intensity_follows_local_lead():
         run = Run(cfg, shards, B)
         run(mode="unfused")
         ref = run.C.clone()
-        trace = torch.zeros(152 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+        trace = trace_buffer(_lib.TRACE_WORDS)
         run.C.zero_()
         run(trace=trace)
         assert torch.equal(run.C, ref), label
@@ -391,17 +394,18 @@ def test_stress_random_orders_delays_pivots_bit_exact():
     run(mode="unfused")
     ref = run.C.clone()
     g = torch.Generator().manual_seed(78)
-    pivots = ["page", "shard", "none", "ready_queue"]
+    pivots = ["page", "shard", "none", "ready_queue", "auto"]
     for i in range(150):
         order = torch.randperm(cfg.nblocks, generator=g).tolist()
         delay = torch.randint(0, 5000, (cfg.nblocks,), generator=g).tolist() if i % 3 == 0 else None
-        pivot = pivots[int(torch.randint(0, 4, (1,), generator=g))]
+        pivot = pivots[int(torch.randint(0, len(pivots), (1,), generator=g))]
         rank = int(torch.randint(0, cfg.R, (1,), generator=g))
         grid = [0, 2, 8, 40][int(torch.randint(0, 4, (1,), generator=g))]
+        band_n = [0, -1, 1, 3][int(torch.randint(0, 4, (1,), generator=g))]
         run.a.view(torch.int16).fill_(-1)
         run.C.zero_()
-        run(order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid)
-        assert torch.equal(run.C, ref), (i, pivot, rank, grid)
+        run(order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n)
+        assert torch.equal(run.C, ref), (i, pivot, rank, grid, band_n)
         assert torch.equal(run.a, torch.cat(run.shards)), i
     # status word, ticket dispenser and per-block counters are zero again (the workspace also
     # keeps the device copies of the last order / delay arrays, which need no clearing)
@@ -460,8 +464,9 @@ def test_soak_random_shapes_orders_modes_bit_exact():
             pivot = pick(["page", "shard", "none", "ready_queue"])
             rank = int(torch.randint(0, R, (1,), generator=g))
             grid = pick([0, 2, 16, 64])
+            band_n = pick([0, -1, 2, 16])
             run.a.view(torch.int16).fill_(-1)
             run.C.zero_()
-            run(mode=mode, order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid)
-            assert torch.equal(run.C, ref), (shape_i, it, mode, pivot, rank, grid)
+            run(mode=mode, order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n)
+            assert torch.equal(run.C, ref), (shape_i, it, mode, pivot, rank, grid, band_n)
             assert torch.equal(run.a, cat), (shape_i, it)

@@ -153,6 +153,35 @@ def test_progress_release(H, W, chunk_rows, D0):
     assert torch.all(counters == 0)
 
 
+@pytest.mark.parametrize("src_off,dst_off,es", [(8, 8, 2), (4, 12, 4), (2, 6, 2), (16, 48, 4), (1, 3, 1)])
+def test_progress_release_misaligned_views(src_off, dst_off, es):
+    """Per-chunk release with sources and destination at byte offsets that allow 16-byte
+    vectors only, 8-byte ones, or element copies, ragged rows: bytes and flags exact."""
+    nranks, D0, H, W, chunk_rows = 4, 2, 203, 131, 40
+    dt = {1: torch.uint8, 2: torch.float16, 4: torch.int32}[es]  # compared as raw bytes
+    g = torch.Generator().manual_seed(src_off * 31 + dst_off)
+    n = D0 * H * W
+    srcs_h = [torch.randint(0, 256, (n * es,), generator=g, dtype=torch.int64).to(torch.uint8)
+              for _ in range(nranks)]
+    srcs = []
+    for sh in srcs_h:
+        buf = torch.zeros(n * es + 64, dtype=torch.uint8, device=DEV)
+        buf[src_off:src_off + n * es].copy_(sh.to(DEV))
+        srcs.append(buf[src_off:src_off + n * es].view(dt).view(D0, 1, 1, H, W))
+    dbuf = torch.zeros(nranks * n * es + 64, dtype=torch.uint8, device=DEV)
+    dst = dbuf[dst_off:dst_off + nranks * n * es].view(dt).view(D0, 1, 1, nranks * H, W)
+    S = -(-H // chunk_rows)
+    progress = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    counters = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows, epoch=5)
+    torch.cuda.synchronize()
+    ref = oracle.tgather([sh.numpy().view({1: np.uint8, 2: np.uint16, 4: np.int32}[es]).reshape(D0, 1, 1, H, W)
+                          for sh in srcs_h])
+    assert _bytes(dst) == ref.tobytes()
+    assert torch.all(dbuf[:dst_off] == 0) and torch.all(dbuf[dst_off + nranks * n * es:] == 0)
+    assert torch.all(progress == 5) and torch.all(counters == 0)
+
+
 @pytest.mark.parametrize("nranks,shape,dtype", [
     (64, (1, 1, 1, 3, 5), torch.int32),       # the maximum rank count
     (64, (2, 1, 1, 17, 128), torch.float16),

@@ -18,16 +18,16 @@ TGC_OK = 0
 TGC_ERR_INVALID_ARG = -1
 TGC_ERR_DTYPE = -2
 TGC_ERR_ALIGN = -3
-TGC_ERR_NOT_RESIDENT = -4
 TGC_ERR_CUDA = -5
 TGC_ERR_TIMEOUT = -6
 TGC_ERR_ABORTED = -7
 TGC_ERR_WORKSPACE = -8
 TGC_ERR_TOO_LARGE = -9
-NOALLOC_MAX_BLOCKS = 2048
+NOALLOC_MAX_BLOCKS = 2048      # TGC_NOALLOC_MAX_BLOCKS
+NOALLOC_SCRATCH_BYTES = 65536  # TGC_NOALLOC_SCRATCH_BYTES
 
 MODES = {"fused": 0, "unfused": 1, "mm_only": 2, "fused_ce": 3}
-PIVOTS = {"page": 0, "shard": 1, "none": 2, "ready_queue": 3}
+PIVOTS = {"page": 0, "shard": 1, "none": 2, "ready_queue": 3, "auto": 4}
 OUT_FORMATS = {"bf16": 0, "f8e4m3": 1}
 DTYPES = {
     torch.uint8: 0, torch.int8: 1, torch.float16: 2, torch.bfloat16: 3,
@@ -65,6 +65,7 @@ class AgMatmulArgs(ctypes.Structure):
         ("spin_timeout_ns", ctypes.c_uint64), ("group_m", ctypes.c_int), ("grid", ctypes.c_int),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("d_status", _vp),
         ("sync", ctypes.c_int), ("stream", _vp), ("trace", _vp), ("out_format", ctypes.c_int),
+        ("trace_words", ctypes.c_size_t), ("band_n", ctypes.c_int),
     ]
 
 
@@ -111,7 +112,7 @@ def load_library(path: str) -> ctypes.CDLL:
     L.tgc_ag_matmul_workspace_bytes.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64]
     L.tgc_ag_matmul_workspace_bytes.restype = ctypes.c_size_t
     L.tgc_ag_matmul_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(_i64), _i64]
     L.tgc_ag_matmul_schedule.restype = _i64
     L.tgc_gemm_tile_shape.argtypes = [ctypes.POINTER(ctypes.c_int)] * 3
@@ -236,7 +237,7 @@ def tgc_ag_matmul_workspace_bytes(nranks: int, M: int, K: int, N: int, comm_bloc
 
 def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | None = None, rank: int = 0,
                      mode: str = "fused", pivot: str = "page", progress=None, epoch: int = 1, order=None,
-                     delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, grid: int = 0,
+                     delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, band_n: int = 0, grid: int = 0,
                      workspace=None, d_status=None, sync: bool = False, stream=None, trace=None,
                      out_format: str = "bf16", check: bool = True) -> int:
     """Extended AllGather-MatMul (see tgc.h).  ``order`` / ``delay_ns`` are host sequences."""
@@ -259,21 +260,23 @@ def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | No
         a_shards=shards, nranks=R, B=_ptr(B), C=_ptr(C), a_out=_ptr(a_out), M=M, K=K, N=N,
         comm_block_rows=comm_block_rows, rank=rank, mode=MODES[mode], pivot=PIVOTS[pivot],
         progress=_ptr(progress), epoch=epoch, order=order_arr, n_order=n_order, delay_ns=delay_arr,
-        spin_timeout_ns=spin_timeout_ns, group_m=group_m, grid=grid, workspace=_ptr(workspace),
+        spin_timeout_ns=spin_timeout_ns, group_m=group_m, band_n=band_n, grid=grid, workspace=_ptr(workspace),
         workspace_bytes=(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream), trace=_ptr(trace),
-        out_format=OUT_FORMATS[out_format])
+        out_format=OUT_FORMATS[out_format],
+        trace_words=(trace.numel() * trace.element_size() // 8) if trace is not None else 0)
     rc = lib().tgc_ag_matmul_ex(ctypes.byref(a))
     return _check(rc, "tgc_ag_matmul_ex") if check else rc
 
 
 def tgc_ag_matmul_schedule(M: int, N: int, comm_block_rows: int, nranks: int, rank: int = 0,
-                           pivot: str = "page", group_m: int = 0, grid: int = 1, cta: int = 0):
-    """Tile sequence (pid_m, pid_n) of persistent CTA ``cta`` (host-side copy of the device schedule)."""
-    n = lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, grid,
-                                     cta, None, 0)
+                           pivot: str = "page", group_m: int = 0, grid: int = 1, cta: int = 0, band_n: int = 0):
+    """Tile sequence (pid_m, pid_n) of persistent CTA ``cta`` (host-side copy of the device schedule);
+    ``band_n`` > 0 selects the band raster."""
+    n = lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, band_n,
+                                     grid, cta, None, 0)
     _check(int(n) if n < 0 else 0, "tgc_ag_matmul_schedule")
     buf = (_i64 * max(1, 2 * n))()
-    lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, grid, cta,
-                                 buf, n)
+    lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, band_n, grid,
+                                 cta, buf, n)
     return [(buf[2 * i], buf[2 * i + 1]) for i in range(n)]

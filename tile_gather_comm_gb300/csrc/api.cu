@@ -73,7 +73,8 @@ static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintp
 
 // Memory pool of the allocating entry point, one per device, owned by the
 // library so that its release threshold does not change the device's default
-// pool.  Memory freed back to it stays mapped for the next call.
+// pool.  Up to TGC_POOL_KEEP_BYTES of memory freed back to it stays mapped for
+// the next call; the rest goes back to the device at the next synchronization.
 static cudaError_t library_pool(int device, cudaMemPool_t *out) {
     static std::mutex mu;
     static std::vector<cudaMemPool_t> pools;
@@ -88,7 +89,7 @@ static cudaError_t library_pool(int device, cudaMemPool_t *out) {
         cudaMemPool_t pool = nullptr;
         cudaError_t e = cudaMemPoolCreate(&pool, &props);
         if (e != cudaSuccess) return e;
-        uint64_t keep = UINT64_MAX;
+        uint64_t keep = TGC_POOL_KEEP_BYTES;
         e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
         if (e != cudaSuccess) return e;
         pools[device] = pool;
@@ -149,7 +150,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
         return TGC_ERR_INVALID_ARG;
     const bool flagged = a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE;
     if (a.pivot != TGC_PIVOT_PAGE && a.pivot != TGC_PIVOT_SHARD && a.pivot != TGC_PIVOT_NONE &&
-        a.pivot != TGC_PIVOT_READY_QUEUE)
+        a.pivot != TGC_PIVOT_READY_QUEUE && a.pivot != TGC_PIVOT_AUTO)
         return TGC_ERR_INVALID_ARG;
     if (a.M % a.nranks != 0) return TGC_ERR_INVALID_ARG;
     const int64_t rows_per_rank = a.M / a.nranks;
@@ -200,6 +201,8 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     }
     if (a.d_status != nullptr && !aligned(a.d_status, 4)) return TGC_ERR_ALIGN;
     if (a.trace != nullptr && !aligned(a.trace, 8)) return TGC_ERR_ALIGN;
+    // a trace holds at least one CTA pair's records (the full bound needs the SM count)
+    if (a.trace != nullptr && a.trace_words < 2 * (size_t)TGC_TRACE_WORDS) return TGC_ERR_INVALID_ARG;
     return 0;
 }
 
@@ -314,6 +317,17 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     cudaStream_t st = a.stream;
     const uint64_t timeout = a.spin_timeout_ns ? a.spin_timeout_ns : 2000000000ull;
 
+    if (a.trace != nullptr) {
+        // one trace record per launched CTA: CTAs come in pairs, at most one per SM, and no
+        // more than `grid` (at least one pair) when the caller sets it
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int sms = sm_count(dev);
+        const int want = a.grid > 0 ? (a.grid < 2 ? 2 : a.grid) : sms;
+        const int ctas = want < sms ? want : sms;
+        if (a.trace_words < (size_t)ctas * TGC_TRACE_WORDS) return TGC_ERR_INVALID_ARG;
+    }
     int32_t *status = a.d_status;
     WorkspaceLayout wl = workspace_layout(chk.nblocks, tile_rows_of(a.M));
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -333,10 +347,29 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.N = a.N;
     G.cb = a.comm_block_rows;
     G.rank = a.rank;
-    G.pivot = (a.pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED)
-                  ? (a.mode == TGC_MODE_FUSED_CE ? (int)TGC_PIVOT_PAGE : (int)TGC_PIVOT_NONE)
-                  : (int)a.pivot;
+    const bool flagged = a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE;
     G.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
+    // Raster.  The fused modes take the band raster when the caller's shard holds fewer tile
+    // rows than one group of the group raster: that raster's first group would already wait
+    // on remote rows all at once, while bands ask for them one tile row at a time.  With a
+    // longer local lead the group raster consumes remote rows slowly enough for the copy to
+    // stay ahead, and keeps its operand reuse.
+    if (a.band_n > 0) G.band_n = a.band_n;
+    else if (a.band_n < 0 || !flagged) G.band_n = 0;
+    else G.band_n = chk.rows_per_rank / kTileM < G.group_m ? TGC_DEFAULT_BAND_N : 0;
+    // Tile order.  AUTO: the ready order for FUSED when the caller gives a release order and
+    // the band raster walks rows soon enough to meet it out of order; the page's rank pivot
+    // otherwise (with the default release order both orders coincide, and the ready order
+    // only adds its ring lookups).
+    tgc_pivot pivot = a.pivot;
+    if (pivot == TGC_PIVOT_AUTO)
+        pivot = a.mode == TGC_MODE_FUSED ? (a.order != nullptr && G.band_n > 0 ? TGC_PIVOT_READY_QUEUE
+                                                                                : TGC_PIVOT_PAGE)
+              : a.mode == TGC_MODE_FUSED_CE ? TGC_PIVOT_PAGE
+                                            : TGC_PIVOT_NONE;
+    G.pivot = (pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED)
+                  ? (a.mode == TGC_MODE_FUSED_CE ? (int)TGC_PIVOT_PAGE : (int)TGC_PIVOT_NONE)
+                  : (int)pivot;
     G.grid = a.grid;
     G.timeout_ns = timeout;
     G.status = status;
@@ -485,7 +518,7 @@ int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *
     a.N = N;
     a.comm_block_rows = comm_block_rows;
     a.mode = TGC_MODE_FUSED;
-    a.pivot = TGC_PIVOT_PAGE;
+    a.pivot = TGC_PIVOT_AUTO;
     a.epoch = 1;
     a.stream = stream;
     a.sync = 1;
@@ -535,7 +568,8 @@ int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *
 }
 
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks, int rank,
-                               tgc_pivot pivot, int group_m, int grid, int cta, int64_t *out, int64_t max_tiles) {
+                               tgc_pivot pivot, int group_m, int band_n, int grid, int cta, int64_t *out,
+                               int64_t max_tiles) {
     if (M <= 0 || N <= 0 || nranks <= 0 || M % nranks != 0 || rank < 0 || rank >= nranks || grid <= 0 ||
         cta < 0 || cta >= grid || group_m < 0 || comm_block_rows <= 0)
         return TGC_ERR_INVALID_ARG;
@@ -545,6 +579,7 @@ int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, in
     s.num_pid_n = (int)((N + kBN - 1) / kBN);
     s.num_tiles = s.num_pid_m * s.num_pid_n;
     s.group_m = group_m > 0 ? group_m : TGC_DEFAULT_GROUP_M;
+    s.band_n = band_n > 0 ? band_n : 0;
     s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kTileM, s.num_pid_m);
     int64_t n = 0;
     for (int t = cta; t < s.num_tiles; t += grid, ++n) {
@@ -570,7 +605,6 @@ const char *tgc_status_string(int status) {
         case TGC_ERR_INVALID_ARG: return "invalid argument";
         case TGC_ERR_DTYPE: return "unsupported dtype";
         case TGC_ERR_ALIGN: return "misaligned pointer or row pitch";
-        case TGC_ERR_NOT_RESIDENT: return "persistent grid cannot be made resident";
         case TGC_ERR_CUDA: return "CUDA error (see tgc_last_cuda_error)";
         case TGC_ERR_TIMEOUT: return "bounded device wait expired";
         case TGC_ERR_ABORTED: return "kernel aborted after another CTA failed";

@@ -258,6 +258,24 @@ __device__ __forceinline__ TilePos tile_at(const GemmParams &p, int pos) {
         return r;
     }
     const int npn = p.sched.num_pid_n;
+    if (p.sched.band_n > 0) {
+        // band raster: every band walks the caller's own rows, then the ready ring in order
+        const int bn = p.sched.band_n;
+        const int in_band = bn * p.sched.num_pid_m;
+        const int band_id = pos / in_band;
+        const int first_n = band_id * bn;
+        const int bw = (npn - first_n) < bn ? (npn - first_n) : bn;
+        const int rr = pos - band_id * in_band;
+        const int row_idx = rr / bw;
+        r.pid_n = first_n + rr % bw;
+        if (row_idx < p.rq_local_rows) {
+            r.pid_m = p.rq_local_row0 + row_idx;
+        } else {
+            r.ring_idx = row_idx - p.rq_local_rows;
+            r.pid_m = -1;
+        }
+        return r;
+    }
     const int n_local = p.rq_local_rows * npn;
     if (pos < n_local) {
         TileSchedule s = p.sched;
@@ -1055,7 +1073,10 @@ static int copy_warps_for(const GemmParams &p, int nclusters) {
     const int horizon = TGC_COPY_LEAD_WAVES * nclusters;
     bool urgent = false;
     if (p.rq) {
-        urgent = p.rq_local_rows * p.sched.num_pid_n < horizon;
+        // positions of the caller's own rows at the head of the order (of the first band)
+        const int cols = p.sched.band_n > 0 && p.sched.band_n < p.sched.num_pid_n ? p.sched.band_n
+                                                                                 : p.sched.num_pid_n;
+        urgent = p.rq_local_rows * cols < horizon;
     } else {
         for (int t = 0; t < horizon && t < p.sched.num_tiles && !urgent; ++t) {
             int pm = 0, pn = 0;
@@ -1095,6 +1116,7 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     p.sched.num_pid_n = (int)((L.N + kBN - 1) / kBN);
     p.sched.num_tiles = p.sched.num_pid_m * p.sched.num_pid_n;
     p.sched.group_m = L.group_m;
+    p.sched.band_n = L.band_n;
     const int64_t rows_per_rank = L.M / L.nranks;
     p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, C::kTileM, p.sched.num_pid_m);
     p.C = static_cast<uint16_t *>(L.C);
@@ -1110,10 +1132,11 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     const int sms = sm_count(dev);
 
     CUtensorMap tmA, tmL, tmB, tmC;
+    std::memset(&tmC, 0, sizeof tmC);
     if (!make_map(&tmA, L.a, L.M, L.K, C::kRowsCta) || !make_map(&tmB, L.B, L.N, L.K, C::kHalfN))
         return TGC_ERR_CUDA;
-    // (for float8 output the epilogue stores C itself and this map is not used)
-    if (!make_map_c(&tmC, L.C, L.M, L.N)) return TGC_ERR_CUDA;
+    // bf16 C leaves through TMA stores; float8 C is stored by the epilogue itself (no map)
+    if (!L.out_fp8 && !make_map_c(&tmC, L.C, L.M, L.N)) return TGC_ERR_CUDA;
     if (L.fused) {
         if (!make_map(&tmL, L.shards[L.rank], rows_per_rank, L.K, C::kRowsCta)) return TGC_ERR_CUDA;
         p.cb = (int)L.cb;

@@ -59,6 +59,7 @@ struct GemmLaunch {
     int rank;
     int pivot;
     int group_m;
+    int band_n;        // > 0: band raster of band_n tile columns; otherwise the group raster
     int grid;
     uint32_t *progress;
     uint32_t epoch;

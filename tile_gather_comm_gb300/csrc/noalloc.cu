@@ -8,15 +8,15 @@
 // host threads that must never touch the allocator while another thread holds
 // it.  tgc_ag_matmul allocates its temporaries and tgc_ag_matmul_ex needs a
 // caller-allocated workspace and flag array; this entry point instead keeps
-// that scratch -- status word, ticket dispenser, per-block piece counters and
-// per-block progress flags -- in one fixed array in device memory that the
-// library declares statically.  The caller passes only inputs and outputs.
+// that scratch -- status word, ticket dispenser, per-block piece counters,
+// per-block progress flags, per-tile-row counters and the ready ring -- in one
+// fixed array in device memory that the library declares statically.  The
+// caller passes only inputs and outputs.
 //
 // The array is a property of the loaded module: every GPU that loads the
 // library holds kNoAllocScratchBytes of it until the process exits, and every
 // call on a device shares that device's copy.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -24,7 +24,7 @@
 
 namespace tgc {
 
-constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+constexpr size_t kNoAllocScratchBytes = TGC_NOALLOC_SCRATCH_BYTES;
 constexpr int64_t kNoAllocMaxBlocks = TGC_NOALLOC_MAX_BLOCKS;
 
 // The scratch.  Host code must not use this name as an address (on the host
@@ -34,25 +34,15 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-uint8_t *g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch on the current device, looked up once per
-// device with that device current.
+// Device address of the scratch on the current device.  It is looked up on
+// every call (with the caller's device current) rather than cached: the lookup
+// allocates nothing, and a cached address would go stale if the device were
+// reset and the module loaded again.
 int scratch_address(uint8_t **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return TGC_ERR_INVALID_ARG;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e);
-        g_scratch_addr[dev] = static_cast<uint8_t *>(p);
-    }
-    *out = g_scratch_addr[dev];
+    *out = static_cast<uint8_t *>(p);
     return TGC_OK;
 }
 
@@ -90,7 +80,7 @@ extern "C" int tgc_ag_matmul_noalloc(const void *const *a_shards, int nranks, co
     a.comm_block_rows = comm_block_rows;
     a.rank = 0;
     a.mode = TGC_MODE_FUSED;
-    a.pivot = TGC_PIVOT_PAGE;
+    a.pivot = TGC_PIVOT_AUTO;
     a.epoch = 1;
     a.sync = 1;
     a.stream = stream;

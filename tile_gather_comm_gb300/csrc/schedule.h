@@ -26,10 +26,27 @@ struct TileSchedule {
     int num_tiles;
     int group_m;
     int pivot_off;  // in tile rows, already reduced mod num_pid_m
+    int band_n;     // > 0: band raster of band_n tile columns (group_m unused)
 
-    // Linear tile index -> (pid_m, pid_n): group_m tile rows per group,
-    // column-major inside a group, then the rank rotation of pid_m.
+    // Linear tile index -> (pid_m, pid_n), then the rank rotation of pid_m.
+    //   group raster (band_n <= 0): group_m tile rows per group, column-major
+    //       inside a group -- the page's GROUP_SIZE_M swizzle;
+    //   band raster (band_n > 0): band_n tile columns per band, row-major inside
+    //       a band -- every band walks the tile rows in order while its columns
+    //       of B stay in L2, so the rows are needed in the order a producer
+    //       releases them.
     TGC_HD void tile(int t, int &pid_m, int &pid_n) const {
+        if (band_n > 0) {
+            const int in_band = band_n * num_pid_m;
+            const int band_id = t / in_band;
+            const int first_n = band_id * band_n;
+            const int bw = (num_pid_n - first_n) < band_n ? (num_pid_n - first_n) : band_n;
+            const int r = t - band_id * in_band;
+            pid_m = r / bw + pivot_off;
+            pid_n = first_n + r % bw;
+            if (pid_m >= num_pid_m) pid_m -= num_pid_m;
+            return;
+        }
         const int in_group = group_m * num_pid_n;
         const int group_id = t / in_group;
         const int first_m = group_id * group_m;

@@ -54,6 +54,13 @@ namespace tgc {
 #ifndef TGC_TG_VW32
 #define TGC_TG_VW32 1          // flat kernel: 32-byte vectors when every address allows them
 #endif
+#ifndef TGC_TG_REL_PDL
+#define TGC_TG_REL_PDL 1       // release kernel: programmatic dependent launch, as the flat kernel
+#endif
+#ifndef TGC_TG_REL_ATOM
+#define TGC_TG_REL_ATOM 1      // release kernel: thread 0 counts an item with one release atomic (1),
+                               // or with a gpu-scope fence followed by an acq_rel atomic (0)
+#endif
 #ifndef TGC_TG_CHUNK
 #define TGC_TG_CHUNK 32768     // flat kernel: shares above this many bytes are cut into chunks
                                // dealt round-robin over the CTAs (0: one contiguous share each)
@@ -127,7 +134,12 @@ __device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t
 template <int VW>
 __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
     using V = typename VecT<VW>::T;
-    constexpr int64_t kTileVecs = (int64_t)kTGThreads * kTGUnroll;
+    constexpr int U = VW == 32 ? kTGUnroll / 2 : kTGUnroll;  // the same bytes in flight per thread
+    constexpr int64_t kTileVecs = (int64_t)kTGThreads * U;
+#if TGC_TG_REL_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
     const int tid = threadIdx.x;
 
     for (int64_t item = blockIdx.x; item < p.total_items; item += gridDim.x) {
@@ -156,16 +168,16 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
             const V *vs = reinterpret_cast<const V *>(src + head) + v0;
             V *vd = reinterpret_cast<V *>(dst + head) + v0;
             const int64_t n = (nvec - v0) < kTileVecs ? (nvec - v0) : kTileVecs;
-            V reg[kTGUnroll];
+            V reg[U];
 #pragma unroll
-            for (int k = 0; k < kTGUnroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int64_t idx = tid + (int64_t)k * kTGThreads;
                 if (idx < n) reg[k] = ld_stream(vs + idx);
             }
 #pragma unroll
-            for (int k = 0; k < kTGUnroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int64_t idx = tid + (int64_t)k * kTGThreads;
-                if (idx < n) vd[idx] = reg[k];
+                if (idx < n) st_vec(vd + idx, reg[k]);
             }
         }
         if (tile == 0) {
@@ -175,16 +187,24 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
 
         if (p.progress != nullptr) {
             // Publish chunk (r, s) once all its nslab*tiles_per_seg items are written.  The
-            // barrier orders every thread's stores of this item before thread 0, whose gpu-scope
-            // fence then makes them visible before the count; the other threads go on to their
-            // next item instead of each waiting for its own stores (measured +1.5-2%).
+            // barrier orders every thread's stores of this item before thread 0's count; the other
+            // threads go on to their next item instead of each waiting for its own stores.
             __syncthreads();
             if (tid == 0) {
-                __threadfence();
                 const int64_t c = (int64_t)r * p.nseg + s;
                 const uint32_t target = (uint32_t)(p.nslab * p.tiles_per_seg);
+#if TGC_TG_REL_ATOM
+                // the release add makes the item's bytes visible before the count (measured
+                // 4.7% faster on the TGATHER workload than a separate fence and acq_rel add)
+                const uint32_t old = atom_add_release_gpu(p.counters + c, 1u);
+#else
+                __threadfence();
                 const uint32_t old = atom_add_acq_rel_gpu(p.counters + c, 1u);
+#endif
                 if (old + 1 == target) {
+                    // acquire side: the other items' bytes, released by their counts, are
+                    // visible to this thread before it publishes the chunk
+                    __threadfence();
                     st_relaxed_gpu(p.counters + c, 0u);  // no other item of this chunk remains
                     st_release_gpu(p.progress + c, p.epoch);
                 }
@@ -435,9 +455,9 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     p.epoch = L.epoch;
 
     const int vw = pick_vw(L);
-    const int64_t tile_bytes = (int64_t)kTGThreads * kTGUnroll * vw;
+    const int64_t tile_vecs = (int64_t)kTGThreads * (vw == 32 ? kTGUnroll / 2 : kTGUnroll);  // the kernel's kTileVecs
     const int64_t max_vecs = L.seg_bytes / vw;
-    p.tiles_per_seg = max_vecs > 0 ? (max_vecs + (tile_bytes / vw) - 1) / (tile_bytes / vw) : 1;
+    p.tiles_per_seg = max_vecs > 0 ? (max_vecs + tile_vecs - 1) / tile_vecs : 1;
     if (p.tiles_per_seg < 1) p.tiles_per_seg = 1;
     p.total_items = L.nseg * (int64_t)L.nranks * L.nslab * p.tiles_per_seg;
 
@@ -486,14 +506,23 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     const int64_t waves = (p.total_items + slots - 1) / slots;
     const int64_t grid = (p.total_items + waves - 1) / waves;
 
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kTGThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = TGC_TG_REL_PDL ? 1 : 0;
     switch (vw) {
-        case 16: tgather_kernel<16><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
-        case 8: tgather_kernel<8><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
-        case 4: tgather_kernel<4><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
-        case 2: tgather_kernel<2><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
-        default: tgather_kernel<1><<<(unsigned)grid, kTGThreads, 0, stream>>>(p); break;
+        case 16: e = cudaLaunchKernelEx(&cfg, tgather_kernel<16>, p); break;
+        case 8: e = cudaLaunchKernelEx(&cfg, tgather_kernel<8>, p); break;
+        case 4: e = cudaLaunchKernelEx(&cfg, tgather_kernel<4>, p); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, tgather_kernel<2>, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, tgather_kernel<1>, p); break;
     }
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
 
