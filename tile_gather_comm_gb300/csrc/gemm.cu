@@ -1094,11 +1094,14 @@ static int copy_warps_for(const GemmParams &p, int nclusters) {
 // small gather spread over many warps then finishes in a few round trips
 // instead of one long piece per warp; a large one keeps the per-piece fence
 // and counter traffic low.
+#ifndef TGC_PIECES_PER_WARP
+#define TGC_PIECES_PER_WARP 2
+#endif
 static int piece_bytes_for(const GemmParams &p, int64_t copy_warps_total) {
     int pb = kMaxPieceBytes;
     while (pb > kMinPieceBytes) {
         const int64_t pieces = (int64_t)p.n_order * ((p.block_bytes + pb - 1) / pb);
-        if (pieces >= 2 * copy_warps_total) break;
+        if (pieces >= TGC_PIECES_PER_WARP * copy_warps_total) break;
         pb /= 2;
     }
     return pb;
