@@ -401,6 +401,48 @@ int tgc_ag_matmul_noalloc(const void *const *a_shards, int nranks, const void *B
                           int64_t M, int64_t K, int64_t N, int64_t comm_block_rows,
                           cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Ranks in separate processes                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [AGM] section 对称内存如何打通GPU间访问: every rank allocates its a_shard (M/W, K) in
+ * memory the other ranks can address, and each rank's producer copies the other ranks'
+ * shards into its own `a` ([AGM] section 数据搬运与细粒度同步).  With one process per
+ * rank, a rank exports the device buffer holding its shard as an IPC handle
+ * (tgc_ipc_export), the ranks exchange the handles by any host transport, and each
+ * rank opens the others' (tgc_ipc_open) to obtain device pointers it passes, in rank
+ * order with its own shard's pointer at its own index, as a_shards[] to
+ * tgc_ag_matmul_ex with `rank` set to itself.  Every rank computes C = a * B_r^T with
+ * its own B_r and publishes its own progress flags; nothing is written into another
+ * rank's memory.  Peer bytes are moved only by the kernels' own loads and stores (the
+ * register-copy producer of FUSED, the TGATHER kernel of UNFUSED) or, in FUSED_CE, by
+ * device-to-device copies; tile loads (TMA) read the caller's own shard, `a` and B,
+ * all local.  The library build that copies with bulk asynchronous copies
+ * (TGC_COPY_LSU=0) would read peer memory with them and must not be used with peer
+ * pointers.
+ *
+ * The caller orders the ranks: a peer's shard must be complete before a rank's call
+ * is enqueued (for instance: every rank synchronizes its writes, then a barrier), and
+ * must not be freed or rewritten until every rank's call has completed.
+ */
+typedef struct tgc_ipc_handle {
+    unsigned char bytes[64];  /* the CUDA IPC handle of the allocation holding the buffer */
+    uint64_t offset;          /* byte offset of the buffer inside that allocation          */
+} tgc_ipc_handle;
+
+/* Fills *out for the device buffer at d_ptr (any address inside an allocation made
+ * with cudaMalloc, in the current device).  TGC_ERR_INVALID_ARG for null arguments,
+ * TGC_ERR_CUDA if the runtime cannot export the allocation (for instance memory from
+ * a virtual-memory or pool allocator). */
+int tgc_ipc_export(const void *d_ptr, tgc_ipc_handle *out);
+/* Maps another process's exported buffer into this process (current device; peer
+ * access enabled lazily when it lives on another device) and returns its address in
+ * *d_ptr_out.  A handle exported by this same process cannot be opened here. */
+int tgc_ipc_open(const tgc_ipc_handle *h, void **d_ptr_out);
+/* Unmaps a buffer opened by tgc_ipc_open: d_ptr as returned there, h as passed there. */
+int tgc_ipc_close(void *d_ptr, const tgc_ipc_handle *h);
+
 /* Bytes of workspace tgc_ag_matmul_ex needs for this problem (>= 256). */
 size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N,
                                      int64_t comm_block_rows);

@@ -163,6 +163,20 @@ def test_plain_ag_matmul_validates_before_allocating():
     assert L.tgc_ag_matmul(arr, 4, FAKE, FAKE, 64, 60, 64, 8, None) == _lib.TGC_ERR_ALIGN
 
 
+def test_ipc_calls_reject_null_arguments_before_any_cuda_call():
+    L = _lib.lib()
+    h = _lib.IpcHandle()
+    p = ctypes.c_void_p()
+    assert ctypes.sizeof(_lib.IpcHandle) == 72   # 64-byte CUDA IPC handle + 8-byte offset
+    assert L.tgc_ipc_export(None, ctypes.byref(h)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_ipc_export(FAKE, None) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_ipc_open(None, ctypes.byref(p)) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_ipc_open(ctypes.byref(h), None) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_ipc_close(None, ctypes.byref(h)) == _lib.TGC_ERR_INVALID_ARG
+    h.offset = FAKE + 1                            # an offset beyond the address itself
+    assert L.tgc_ipc_close(FAKE, ctypes.byref(h)) == _lib.TGC_ERR_INVALID_ARG
+
+
 def test_workspace_bytes_grows_with_blocks():
     a = tgc.tgc_ag_matmul_workspace_bytes(4, 64, 64, 64, 8)
     b = tgc.tgc_ag_matmul_workspace_bytes(4, 32768, 8192, 8192, 512)

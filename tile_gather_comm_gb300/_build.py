@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtgc.so")
-SOURCES = ["api.cu", "tgather.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "tgather.cu", "gemm.cu", "noalloc.cu", "ipc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

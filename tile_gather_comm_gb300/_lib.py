@@ -69,6 +69,11 @@ class AgMatmulArgs(ctypes.Structure):
     ]
 
 
+class IpcHandle(ctypes.Structure):
+    """tgc_ipc_handle: the CUDA IPC handle of an allocation and a buffer's offset inside it."""
+    _fields_ = [("bytes", ctypes.c_ubyte * 64), ("offset", ctypes.c_uint64)]
+
+
 class TGCError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -109,6 +114,12 @@ def load_library(path: str) -> ctypes.CDLL:
     L.tgc_ag_matmul_noalloc.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _vp]
     L.tgc_ag_matmul_noalloc.restype = ctypes.c_int
+    L.tgc_ipc_export.argtypes = [_vp, ctypes.POINTER(IpcHandle)]
+    L.tgc_ipc_export.restype = ctypes.c_int
+    L.tgc_ipc_open.argtypes = [ctypes.POINTER(IpcHandle), ctypes.POINTER(_vp)]
+    L.tgc_ipc_open.restype = ctypes.c_int
+    L.tgc_ipc_close.argtypes = [_vp, ctypes.POINTER(IpcHandle)]
+    L.tgc_ipc_close.restype = ctypes.c_int
     L.tgc_ag_matmul_workspace_bytes.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64]
     L.tgc_ag_matmul_workspace_bytes.restype = ctypes.c_size_t
     L.tgc_ag_matmul_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -229,6 +240,26 @@ def tgc_ag_matmul_noalloc(a_shards, B, C, a_out, comm_block_rows: int, stream=No
     rc = lib().tgc_ag_matmul_noalloc(_ptrs(a_shards), R, _ptr(B), _ptr(C), _ptr(a_out), R * H, K, N,
                                      comm_block_rows, _stream(stream))
     return _check(rc, "tgc_ag_matmul_noalloc") if check else rc
+
+
+def tgc_ipc_export(buf) -> bytes:
+    """The tgc_ipc_handle of a device buffer (tensor or address), as bytes to send to the other ranks."""
+    h = IpcHandle()
+    _check(lib().tgc_ipc_export(_ptr(buf), ctypes.byref(h)), "tgc_ipc_export")
+    return bytes(h)
+
+
+def tgc_ipc_open(handle: bytes) -> int:
+    """Address, in this process, of a buffer another process exported."""
+    h = IpcHandle.from_buffer_copy(handle)
+    p = _vp()
+    _check(lib().tgc_ipc_open(ctypes.byref(h), ctypes.byref(p)), "tgc_ipc_open")
+    return int(p.value)
+
+
+def tgc_ipc_close(ptr: int, handle: bytes) -> None:
+    h = IpcHandle.from_buffer_copy(handle)
+    _check(lib().tgc_ipc_close(ptr, ctypes.byref(h)), "tgc_ipc_close")
 
 
 def tgc_ag_matmul_workspace_bytes(nranks: int, M: int, K: int, N: int, comm_block_rows: int) -> int:
