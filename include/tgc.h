@@ -364,6 +364,23 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 #define TGC_TRACE_COPY_WARPS 13  /* producer: warps of this CTA that took pieces     */
 
 /*
+ * The tile order and raster a call to tgc_ag_matmul_ex with these arguments runs,
+ * with TGC_PIVOT_AUTO and band_n = 0 resolved as described above: pivot is PAGE,
+ * SHARD, NONE or READY_QUEUE; band_n > 0 means the band raster of that many tile
+ * columns, 0 the group raster of group_m tile rows.  The arguments are checked as
+ * tgc_ag_matmul_ex checks them (the same negative status for invalid ones), but
+ * nothing is enqueued and no pointer is dereferenced: placeholders will do.  Needs
+ * no GPU.
+ */
+typedef struct tgc_ag_matmul_plan_t {
+    tgc_pivot pivot;
+    int band_n;
+    int group_m;
+} tgc_ag_matmul_plan_t;
+
+int tgc_ag_matmul_plan(const tgc_ag_matmul_args *args, tgc_ag_matmul_plan_t *out);
+
+/*
  * tgc_ag_matmul_noalloc -- the fused AllGather-MatMul of tgc_ag_matmul with
  * no device allocation.  No counterpart on the pages: this is a library
  * convenience for callers that cannot call cudaMalloc -- for instance code

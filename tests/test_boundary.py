@@ -149,6 +149,45 @@ def test_status_codes_match_header_and_unused_code_is_unknown():
     assert tgc.tgc_status_string(-4) == "unknown status"
 
 
+def _plan(**kw):
+    R = kw.pop("R", 4)
+    args = dict(a_shards=(ctypes.c_void_p * R)(*([FAKE] * R)), nranks=R, B=FAKE, C=FAKE, a_out=FAKE,
+                M=64, K=64, N=64, comm_block_rows=8, rank=0, mode=0, pivot=4, progress=FAKE, epoch=1,
+                workspace=FAKE, workspace_bytes=1 << 30, sync=0)
+    args.update(kw)
+    out = _lib.AgMatmulPlan()
+    rc = _lib.lib().tgc_ag_matmul_plan(ctypes.byref(_lib.AgMatmulArgs(**args)), ctypes.byref(out))
+    return rc, (out.pivot, out.band_n, out.group_m)
+
+
+def test_auto_order_and_raster_follow_the_measured_rule():
+    """AUTO and band_n = 0, resolved without a GPU: bands of 16 tile columns for the fused modes when
+    a shard holds fewer 256-row tile rows than a group (8), the group raster otherwise; the ready
+    order only with an explicit release order on the band raster, the page pivot otherwise."""
+    P = _lib.PIVOTS
+    order = (ctypes.c_int32 * 2)(1, 0)
+    square = dict(R=8, M=4096, K=4096, N=4096, comm_block_rows=128)
+    mlp_up = dict(R=8, M=8192, K=4096, N=14336, comm_block_rows=256)
+    large = dict(R=4, M=32768, K=8192, N=8192, comm_block_rows=512)
+    assert _plan(**square) == (0, (P["page"], 16, 8))
+    assert _plan(**mlp_up) == (0, (P["page"], 16, 8))
+    assert _plan(**large) == (0, (P["page"], 0, 8))
+    assert _plan(**square, order=order, n_order=2) == (0, (P["ready_queue"], 16, 8))
+    assert _plan(**large, order=order, n_order=2) == (0, (P["page"], 0, 8))   # group raster: page
+    assert _plan(**square, group_m=2) == (0, (P["page"], 0, 2))               # 2 tile rows, not < 2
+    assert _plan(**square, band_n=-1) == (0, (P["page"], 0, 8))
+    assert _plan(**large, band_n=5) == (0, (P["page"], 5, 8))
+    assert _plan(**square, mode=_lib.MODES["fused_ce"], order=order, n_order=2) == (0, (P["page"], 16, 8))
+    for mode in ("unfused", "mm_only"):
+        assert _plan(**square, mode=_lib.MODES[mode]) == (0, (P["none"], 0, 8))
+        assert _plan(**square, mode=_lib.MODES[mode], pivot=P["ready_queue"]) == (0, (P["none"], 0, 8))
+    assert _plan(**square, pivot=P["shard"]) == (0, (P["shard"], 16, 8))
+    # the same argument checks as the call itself
+    assert _plan(**dict(square, M=4097))[0] == _lib.TGC_ERR_INVALID_ARG
+    assert _plan(**dict(square, K=60))[0] == _lib.TGC_ERR_ALIGN
+    assert _lib.lib().tgc_ag_matmul_plan(None, None) == _lib.TGC_ERR_INVALID_ARG
+
+
 def test_ag_matmul_empty_problem_is_ok():
     assert _ag(M=0, B=None, C=None, a_out=None) == _lib.TGC_OK
     assert _ag(N=0, B=None, C=None, a_out=None) == _lib.TGC_OK

@@ -74,6 +74,10 @@ class IpcHandle(ctypes.Structure):
     _fields_ = [("bytes", ctypes.c_ubyte * 64), ("offset", ctypes.c_uint64)]
 
 
+class AgMatmulPlan(ctypes.Structure):
+    _fields_ = [("pivot", ctypes.c_int), ("band_n", ctypes.c_int), ("group_m", ctypes.c_int)]
+
+
 class TGCError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -111,6 +115,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.tgc_ag_matmul.restype = ctypes.c_int
     L.tgc_ag_matmul_ex.argtypes = [ctypes.POINTER(AgMatmulArgs)]
     L.tgc_ag_matmul_ex.restype = ctypes.c_int
+    L.tgc_ag_matmul_plan.argtypes = [ctypes.POINTER(AgMatmulArgs), ctypes.POINTER(AgMatmulPlan)]
+    L.tgc_ag_matmul_plan.restype = ctypes.c_int
     L.tgc_ag_matmul_noalloc.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _vp]
     L.tgc_ag_matmul_noalloc.restype = ctypes.c_int

@@ -206,6 +206,43 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     return 0;
 }
 
+// The tile order and raster a call runs (the resolution of AUTO and of band_n = 0).
+struct OrderPlan {
+    int pivot;    // PAGE / SHARD / NONE / READY_QUEUE as the kernel takes it
+    int band_n;   // > 0: band raster of band_n tile columns; 0: group raster
+    int group_m;  // tile rows per group of the group raster
+};
+
+static OrderPlan resolve_order(const tgc_ag_matmul_args &a, const AGCheck &chk) {
+    OrderPlan o{};
+    const bool flagged = a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE;
+    o.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
+    // Raster.  The fused modes take the band raster when the caller's shard holds fewer tile
+    // rows than one group of the group raster: that raster's first group would already wait
+    // on remote rows all at once, while bands ask for them one tile row at a time.  With a
+    // longer local lead the group raster consumes remote rows slowly enough for the copy to
+    // stay ahead, and keeps its operand reuse.
+    if (a.band_n > 0) o.band_n = a.band_n;
+    else if (a.band_n < 0 || !flagged) o.band_n = 0;
+    else o.band_n = chk.rows_per_rank / kTileM < o.group_m ? TGC_DEFAULT_BAND_N : 0;
+    // Tile order.  AUTO: the ready order for FUSED when the caller gives a release order and
+    // the band raster walks rows soon enough to meet it out of order; the page's rank pivot
+    // otherwise (with the default release order both orders coincide, and the ready order
+    // only adds its ring lookups).
+    tgc_pivot pivot = a.pivot;
+    if (pivot == TGC_PIVOT_AUTO)
+        pivot = a.mode == TGC_MODE_FUSED ? (a.order != nullptr && o.band_n > 0 ? TGC_PIVOT_READY_QUEUE
+                                                                                : TGC_PIVOT_PAGE)
+              : a.mode == TGC_MODE_FUSED_CE ? TGC_PIVOT_PAGE
+                                            : TGC_PIVOT_NONE;
+    // the ready order needs the in-kernel producer: the copy-engine mode takes the page pivot,
+    // the plain GEMM no rotation
+    o.pivot = (pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED)
+                  ? (a.mode == TGC_MODE_FUSED_CE ? (int)TGC_PIVOT_PAGE : (int)TGC_PIVOT_NONE)
+                  : (int)pivot;
+    return o;
+}
+
 // ------------------------------------------------------------------ copy-engine producer
 
 using WriteValue32Fn = PFN_cuStreamWriteValue32_v11070;
@@ -347,29 +384,10 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     G.N = a.N;
     G.cb = a.comm_block_rows;
     G.rank = a.rank;
-    const bool flagged = a.mode == TGC_MODE_FUSED || a.mode == TGC_MODE_FUSED_CE;
-    G.group_m = a.group_m > 0 ? a.group_m : TGC_DEFAULT_GROUP_M;
-    // Raster.  The fused modes take the band raster when the caller's shard holds fewer tile
-    // rows than one group of the group raster: that raster's first group would already wait
-    // on remote rows all at once, while bands ask for them one tile row at a time.  With a
-    // longer local lead the group raster consumes remote rows slowly enough for the copy to
-    // stay ahead, and keeps its operand reuse.
-    if (a.band_n > 0) G.band_n = a.band_n;
-    else if (a.band_n < 0 || !flagged) G.band_n = 0;
-    else G.band_n = chk.rows_per_rank / kTileM < G.group_m ? TGC_DEFAULT_BAND_N : 0;
-    // Tile order.  AUTO: the ready order for FUSED when the caller gives a release order and
-    // the band raster walks rows soon enough to meet it out of order; the page's rank pivot
-    // otherwise (with the default release order both orders coincide, and the ready order
-    // only adds its ring lookups).
-    tgc_pivot pivot = a.pivot;
-    if (pivot == TGC_PIVOT_AUTO)
-        pivot = a.mode == TGC_MODE_FUSED ? (a.order != nullptr && G.band_n > 0 ? TGC_PIVOT_READY_QUEUE
-                                                                                : TGC_PIVOT_PAGE)
-              : a.mode == TGC_MODE_FUSED_CE ? TGC_PIVOT_PAGE
-                                            : TGC_PIVOT_NONE;
-    G.pivot = (pivot == TGC_PIVOT_READY_QUEUE && a.mode != TGC_MODE_FUSED)
-                  ? (a.mode == TGC_MODE_FUSED_CE ? (int)TGC_PIVOT_PAGE : (int)TGC_PIVOT_NONE)
-                  : (int)pivot;
+    const OrderPlan plan = resolve_order(a, chk);
+    G.group_m = plan.group_m;
+    G.band_n = plan.band_n;
+    G.pivot = plan.pivot;
     G.grid = a.grid;
     G.timeout_ns = timeout;
     G.status = status;
@@ -504,6 +522,18 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args) {
     if (args == nullptr) return TGC_ERR_INVALID_ARG;
     return ag_ex_impl(*args);
+}
+
+int tgc_ag_matmul_plan(const tgc_ag_matmul_args *args, tgc_ag_matmul_plan_t *out) {
+    if (args == nullptr || out == nullptr) return TGC_ERR_INVALID_ARG;
+    AGCheck chk{};
+    const int rc = ag_validate(*args, chk);
+    if (rc < 0) return rc;
+    const OrderPlan o = resolve_order(*args, chk);
+    out->pivot = (tgc_pivot)o.pivot;
+    out->band_n = o.band_n;
+    out->group_m = o.group_m;
+    return TGC_OK;
 }
 
 int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *C, int64_t M, int64_t K, int64_t N,
