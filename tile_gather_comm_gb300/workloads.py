@@ -11,7 +11,7 @@ bf16 by torch.  The release schedule of the skewed workload (order and
 delays) comes from a second generator seeded with ``seed``, so the data do
 not depend on whether the schedule is drawn.
 
-Shapes follow the pages' problem statement ("Triton第四课：基于对称内存融合
+Shapes follow the pages' setting ("Triton第四课：基于对称内存融合
 AllGather 与 MatMul", section 对称内存如何打通GPU间访问: a_shard (M/W, K) bf16,
 b = randn(k, n).T.contiguous() stored (N, K); "CANN PTO-ISA TGATHER 指令深度解析",
 §二 and §九: per-rank (D0, D1, D2, H, W) sources).
