@@ -8,7 +8,7 @@
 // GPU design.  With dense tensors, the H*W elements of rank r in slab
 // (d0,d1,d2) are ONE contiguous run in the source and ONE contiguous run in
 // the destination, so the whole gather is nranks*D0*D1*D2 contiguous copies.
-// Without progress release (tgather_flat_kernel) each CTA of one full wave
+// Without progress release (tgather_flat_kernel) each CTA of a grid of 8 per SM
 // copies an equal byte share of the concatenated runs.  With progress release
 // (tgather_kernel) each run is cut into segments, one per progress chunk, each
 // segment into tiles of kTGThreads*kTGUnroll vectors, and a persistent grid
@@ -49,7 +49,7 @@ namespace tgc {
 #define TGC_TG_MIN_SHARE 4096  // smallest byte share per CTA of the flat kernel
 #endif
 #ifndef TGC_TG_CTAS_PER_SM
-#define TGC_TG_CTAS_PER_SM 8   // CTAs per SM in one wave
+#define TGC_TG_CTAS_PER_SM 8   // CTAs per SM in the grid (5 of them resident at once at 46-47 registers)
 #endif
 #ifndef TGC_TG_VW32
 #define TGC_TG_VW32 1          // flat kernel: 32-byte vectors when every address allows them
@@ -215,8 +215,8 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
 
 // Flat variant (no progress release): the work space is the concatenation of
 // all (slab, rank) runs, cut into gridDim.x equal, 32-byte-aligned shares --
-// every CTA of the one full wave moves the same number of bytes, so they
-// finish together.  A share larger than TGC_TG_CHUNK is dealt as chunks
+// every CTA of the grid moves the same number of bytes, so the SMs get even
+// loads.  A share larger than TGC_TG_CHUNK is dealt as chunks
 // instead: CTA c copies chunks c, c + gridDim.x, ..., so at any moment the
 // grid works on one compact window of memory rather than on gridDim.x far-apart
 // streams (measured: 6.38 vs 6.02 TB/s on 537 MB, unchanged on 67 MB).  A
@@ -467,7 +467,7 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     const int64_t slots = (int64_t)sm_count(dev) * TGC_TG_CTAS_PER_SM;
 
     if (TGC_TG_FLAT && L.progress == nullptr) {
-        // equal 16-byte-aligned shares over one full wave (fewer CTAs only for small copies)
+        // equal 32-byte-aligned shares over 8 CTAs per SM (fewer CTAs only for small copies)
         const int64_t total = L.nslab * L.nranks * L.run_bytes;
         const int64_t min_share = TGC_TG_MIN_SHARE;
         int64_t grid = (total + min_share - 1) / min_share;
