@@ -336,6 +336,7 @@ def run_ours(args, dist: Dist):
         res["tgather_ragged_i32"] = bench_tgather(TG_CONFIGS["ragged_i32"], dev, stream, dist, peaks,
                                                   peaks_kind, args)
         res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
+        res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         return res
     cfg = AG_CONFIGS[args.workload]
     flops = float(cfg.flops)
@@ -598,7 +599,8 @@ def bench_tgather_strided(tcfg, dev, dist, peaks, peaks_kind, pad: int = 64):
                   f"W+{pad} -> a destination view with row pitch W+{pad}",
         "bytes_per_launch": per_set, "buffer_sets": nsets, "launches_timed": reps * nsets,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(per_gpu / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(per_gpu / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(f"tgather_strided/{tcfg.name}", TGATHER_SOURCES),
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<32>"},
     }
     del sets, g
