@@ -19,9 +19,11 @@
  *     before anything is enqueued.  Errors detected on the device (a bounded
  *     wait that expired) are written to a device status word; the synchronous
  *     entry points read it back and return it.
- *   - The library keeps no state between calls (tensor descriptors are
- *     encoded per call on the host).  It is safe to call from several host
- *     threads.
+ *   - The library keeps no per-problem state between calls: tensor
+ *     descriptors are encoded per call on the host, and what it keeps per
+ *     device (the allocating entry point's memory pool, the copy-engine
+ *     mode's side streams, kernel attributes and SM counts) does not depend
+ *     on the problem.  It is safe to call from several host threads.
  *   - A "virtual rank" is one of `nranks` separate allocations in the same
  *     GPU's memory standing for the shard a rank holds ([AGM] section
  *     对称内存如何打通GPU间访问: every rank holds a_shard of shape (M/W, K)).
