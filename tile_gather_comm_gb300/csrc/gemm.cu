@@ -17,6 +17,12 @@
 //       proceeds; here one warp polls (one lane per covered block) with
 //       ld.acquire.gpu and the wait is bounded.
 //
+// Tile order (schedule.h): the group raster (the page's GROUP_SIZE_M swizzle) or
+// a band raster (bands of tile columns, rows walked in order), then the rank
+// rotation of the tile row; or the ready order, built on the device from the
+// order in which the producer completes tile rows.  The host picks the raster
+// and, for TGC_PIVOT_AUTO, the order (api.cu).
+//
 // Tiles are 256 x 256 outputs computed by a CTA pair (a cluster of 2 CTAs on
 // two SMs, tcgen05 cta_group::2): each CTA holds 128 rows of A and 128 of the
 // 256 columns of B per stage, the even CTA issues the 256 x 256 x 16 MMAs for
