@@ -313,6 +313,11 @@ typedef enum tgc_out_format {
  *                device) -- the SM count when grid is 0; a smaller value is
  *                TGC_ERR_INVALID_ARG.
  * Calls that share a workspace or progress array must not overlap on the GPU.
+ * With sync = 0 and without `order` / `delay_ns` a call can be captured in a
+ * CUDA graph (make one uncaptured call first on the device, so that kernel
+ * attributes are set outside the capture).  The epoch is fixed in the graph,
+ * so capture a reset of the progress entries (for instance a memset to 0)
+ * before the call: each replay then publishes its blocks afresh.
  */
 typedef struct tgc_ag_matmul_args {
     const void *const *a_shards;

@@ -240,6 +240,47 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     assert torch.equal(run.a, torch.cat(run.shards))
 
 
+# ----------------------------------------------------------------------------- CUDA graphs
+
+
+def test_fused_call_replayed_from_a_cuda_graph():
+    """tgc_ag_matmul_ex (sync = 0, no host order arrays) captured in a CUDA graph together with a
+    reset of its progress entries, then replayed on new shard contents each time: every replay
+    gives the oracle's C for the data it ran on, and the gathered `a`."""
+    cfg, shards, B = _custom(4, 256, 512, 776, 64, seed=61)
+    run = Run(cfg, shards, B)
+    run()   # outside the capture: kernel attributes and the occupancy query are set up once
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run.progress.zero_()
+            tgc.tgc_ag_matmul_ex(run.shards, run.B, run.C, run.a, cfg.cb, progress=run.progress, epoch=1,
+                                 workspace=run.ws, stream=s, pivot="auto")
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(62)
+    for i in range(3):
+        new = [torch.randn(cfg.H, cfg.K, generator=gen).to(torch.bfloat16) for _ in range(cfg.R)]
+        for d, h in zip(run.shards, new):
+            d.copy_(h)
+        run.C.fill_(float("nan"))
+        run.a.view(torch.int16).fill_(-1)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        C_ref, a_ref = _oracle_full(new, B)
+        assert_within_tol(run.C, C_ref, f"replay {i}")
+        assert np.array_equal(bits16(run.a), a_ref), f"replay {i}: gathered A"
+        assert torch.all(_ws_zero(run) == 0), f"replay {i}: workspace counters"
+
+
+def _ws_zero(run):
+    # status word, ticket dispenser and per-block counters (the rest of the workspace holds
+    # copies of host arrays and the ready ring, which every call rewrites)
+    return torch.cat([run.ws[:4], run.ws[64:80], run.ws[128:128 + 4 * run.cfg.nblocks]])
+
+
 # ----------------------------------------------------------------------------- edge cases
 
 
