@@ -810,11 +810,24 @@ def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):
     oracle.ag_matmul_rows(sh, Bb, rows)
     dt = time.perf_counter() - t0
     fl = 2.0 * len(rows) * cfg.N * cfg.K
-    return {"value": round(fl / dt * 1e-12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"{len(rows)} rows of C (first and last row of each of the {cfg.nblocks} comm blocks plus "
-                      f"{per_block} seeded random rows of each), all {cfg.N} columns, full K={cfg.K}; "
-                      f"fp32 sequential-k dot products, OpenMP over rows"}
+    out = {"value": round(fl / dt * 1e-12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "seconds": round(dt, 3),
+           "sample": f"{len(rows)} rows of C (first and last row of each of the {cfg.nblocks} comm blocks plus "
+                     f"{per_block} seeded random rows of each), all {cfg.N} columns, full K={cfg.K}; "
+                     f"fp32 sequential-k dot products, OpenMP over rows"}
+    # the same oracle on one host thread, on the first rows of that sample (a few seconds)
+    threads = oracle.num_threads()
+    one = rows[: max(1, min(len(rows), 16))]
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.ag_matmul_rows(sh, Bb, one)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(threads)
+    out["single_thread"] = {"value": round(2.0 * len(one) * cfg.N * cfg.K / dt1 * 1e-12, 6), "unit": "TFLOP/s",
+                            "cores": 1, "seconds": round(dt1, 3), "sample": f"the first {len(one)} rows of that sample"}
+    return out
 
 
 def cpu_baseline_tgather(tcfg, reps: int = 5):
