@@ -333,6 +333,27 @@ def test_trace_records_every_cta():
     assert torch.all(used[:, _lib.TRACE["end"]] >= used[:, _lib.TRACE["start"]])
 
 
+def test_trace_size_is_checked_against_the_launched_ctas():
+    """A trace must hold one record per CTA the call may launch: one per SM with grid 0, at most
+    max(grid, 2) otherwise; a smaller buffer is refused before anything is enqueued."""
+    cfg, shards, B = _custom(4, 256, 128, 512, 64, seed=13)
+    run = Run(cfg, shards, B)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    small = torch.zeros((nsm - 2) * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+    assert run(trace=small, check=False) == _lib.TGC_ERR_INVALID_ARG
+    run.epoch -= 1
+    pair = torch.zeros(2 * _lib.TRACE_WORDS, dtype=torch.int64, device=DEV)
+    assert run(trace=pair, grid=2, check=False) == _lib.TGC_OK
+    assert run(trace=pair, grid=1, check=False) == _lib.TGC_OK      # one pair all the same
+    assert run(trace=pair, grid=4, check=False) == _lib.TGC_ERR_INVALID_ARG
+    t = pair.view(2, _lib.TRACE_WORDS).cpu()
+    assert torch.all(t[:, _lib.TRACE["start"]] > 0)   # both CTAs of the one pair recorded
+    C_ref, _ = _oracle_full(shards, B)
+    run.epoch -= 1
+    run(grid=2)
+    assert_within_tol(run.C, C_ref, "one CTA pair")
+
+
 def test_copy_intensity_follows_local_lead():
     """The producer runs on two warps when the caller's own tiles fill the first two waves of the
     tile order, and on every copy warp when the first waves reach remote rows; the piece size is
