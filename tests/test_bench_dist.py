@@ -113,3 +113,25 @@ def test_strip_comments_keeps_code_and_literals():
     # comment and whitespace edits keep the hash; a code edit changes it
     assert bench.strip_comments(src.replace("trailing", "other words")) == out
     assert bench.strip_comments(src.replace("int b;", "int b2;")) != out
+
+
+def test_profiled_traffic_follows_the_kernel_source_hash(tmp_path, monkeypatch):
+    """roofline.traffic comes from profiles/traffic.json only while the entry's hash matches the
+    kernel sources as compiled; every committed entry names its summary, which exists."""
+    sys.path.insert(0, ROOT)
+    import bench
+    current = bench.sources_sha(bench.TGATHER_SOURCES)
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"k/ok": {"source_sha256_16": current, "dram_bytes_per_launch": 123.0},
+                                "k/stale": {"source_sha256_16": "0" * 16, "dram_bytes_per_launch": 456.0}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.profiled_traffic("k/ok", bench.TGATHER_SOURCES) == 123.0
+    assert bench.profiled_traffic("k/stale", bench.TGATHER_SOURCES) is None
+    assert bench.profiled_traffic("k/missing", bench.TGATHER_SOURCES) is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.json"))
+    assert bench.profiled_traffic("k/ok", bench.TGATHER_SOURCES) is None
+    committed = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for key, entry in committed.items():
+        assert entry["dram_bytes_per_launch"] > 0, key
+        assert os.path.exists(os.path.join(ROOT, "profiles", entry["summary"])), key
+        assert entry["command"].startswith("ncu ") and "--clock-control none" in entry["command"], key
