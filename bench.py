@@ -842,9 +842,20 @@ def cpu_baseline_tgather(tcfg, reps: int = 5):
     for _ in range(reps):
         oracle.tgather(srcs)
     dt = (time.perf_counter() - t0) / reps
-    return {"value": round(tcfg.bytes_moved / dt * 1e-9, 2), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt * reps, 3),
-            "sample": f"the full {tcfg.name} workload ({tcfg.bytes_moved} bytes read + written), {reps} runs"}
+    out = {"value": round(tcfg.bytes_moved / dt * 1e-9, 2), "unit": "GB/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "seconds": round(dt * reps, 3),
+           "sample": f"the full {tcfg.name} workload ({tcfg.bytes_moved} bytes read + written), {reps} runs"}
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.tgather(srcs)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(threads)
+    out["single_thread"] = {"value": round(tcfg.bytes_moved / dt1 * 1e-9, 2), "unit": "GB/s", "cores": 1,
+                            "seconds": round(dt1, 3), "sample": "one run of the same workload"}
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
