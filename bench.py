@@ -459,12 +459,29 @@ def run_ours(args, dist: Dist):
             "peak_source": f"{peaks_kind} cuBLAS bf16 held for seconds under the power cap",
             "note": "the headline step (same call) timed over >= 1.2 s; `value` above is its first "
                     f"{args.steps} steps after {args.warmup} warm-up calls"}
+        # context: cuBLAS's GEMM alone on the already gathered A, right after, over a region
+        # as long, so that both figures are taken at the power cap
+        a_full = torch.cat(shards)
+        t_cb = [0.0, 0.0]
+        ms_cb = time_device(lambda: torch.matmul(a_full, B.T, out=C), n_sus, 3, dist, stream, wall=t_cb)
+        del a_full
+        res["sustained"]["cublas_gemm"] = {
+            "value": round(aggregate(ms_cb, flops, dist)[0], 2), "unit": "TFLOP/s", "steps": n_sus,
+            "region_s": round(t_cb[1] - t_cb[0], 3),
+            "note": "context: torch.matmul (cuBLAS) on the gathered A, same shapes, timed right after the "
+                    "fused region; the fused figure includes the gather, this one does not"}
+        res["sustained"]["fused_over_cublas_gemm"] = round(ms_cb / ms_sus, 4)
     res["clocks"] = sampler.stop(window=tuple(t_value))
     if "sustained" in res and sampler.lines:
         cs = clock_summary(sampler.lines, tuple(t_sus))
         if cs is not None:
             res["sustained"]["clocks"] = {"sm_mhz": cs["sm_mhz"], "samples": cs["samples_in_value_region"],
                                           "reasons": cs["reasons"]}
+        cs = clock_summary(sampler.lines, tuple(t_cb))
+        if cs is not None:
+            res["sustained"]["cublas_gemm"]["clocks"] = {"sm_mhz": cs["sm_mhz"],
+                                                         "samples": cs["samples_in_value_region"],
+                                                         "reasons": cs["reasons"]}
 
     if not args.quick:
         res["other_workloads"] = bench_other_workloads(dev, stream, dist, args, peaks)
@@ -814,7 +831,9 @@ def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):
            "kind": "oracle", "seconds": round(dt, 3),
            "sample": f"{len(rows)} rows of C (first and last row of each of the {cfg.nblocks} comm blocks plus "
                      f"{per_block} seeded random rows of each), all {cfg.N} columns, full K={cfg.K}; "
-                     f"fp32 sequential-k dot products, OpenMP over rows"}
+                     f"fp32 sequential-k dot products, OpenMP over rows",
+           # the whole C at the sampled rate (labelled: not measured)
+           "extrapolated_full_s": round(float(cfg.flops) / (fl / dt), 1)}
     # the same oracle on one host thread, on the first rows of that sample (a few seconds)
     threads = oracle.num_threads()
     one = rows[: max(1, min(len(rows), 16))]
