@@ -83,7 +83,8 @@ typedef enum tgc_dtype {
  * Empty input (any of D0, D1, D2, H, W == 0) returns TGC_OK and writes
  * nothing ([TG] §七: empty data returns before any transfer).
  * Errors: TGC_ERR_INVALID_ARG (nranks not in [1, TGC_MAX_RANKS], negative
- * extent, null pointer), TGC_ERR_DTYPE, TGC_ERR_ALIGN, TGC_ERR_CUDA.
+ * extent, null pointer, or a destination of 2^62 bytes or more),
+ * TGC_ERR_DTYPE, TGC_ERR_ALIGN, TGC_ERR_CUDA.
  * Asynchronous on `stream`.
  */
 int tgc_tgather(void *dst, const void *const *srcs, int nranks,
@@ -105,8 +106,9 @@ int tgc_tgather(void *dst, const void *const *srcs, int nranks,
  * (undefined otherwise).  Rows that are contiguous in both source and
  * destination (ss[4] == ds[4] == 1) are copied with the widest vector every
  * start address and stride allows; otherwise element by element.  Errors and
- * the empty-input rule as tgc_tgather; a negative stride is
- * TGC_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ * the empty-input rule as tgc_tgather; a negative stride, or a view whose last
+ * element lies 2^62 bytes or more from its base, is TGC_ERR_INVALID_ARG.
+ * Asynchronous on `stream`.
  */
 int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const *srcs,
                         const int64_t *src_strides, int nranks,

@@ -61,6 +61,11 @@ def test_tgather_invalid_arguments():
     assert _tg(FAKE, [None], 1, 1, 1, 1, 4, 4) == E.TGC_ERR_INVALID_ARG
     assert _tg(FAKE + 2, [FAKE], 1, 1, 1, 1, 4, 4, dt=5) == E.TGC_ERR_ALIGN   # f32 needs 4-byte alignment
     assert _tg(FAKE, [FAKE, FAKE + 6], 2, 1, 1, 1, 4, 4, dt=6) == E.TGC_ERR_ALIGN
+    # sizes whose byte counts would overflow 64-bit offsets are refused before any launch
+    big = 1 << 31
+    assert _tg(FAKE, [FAKE], 1, big, big, 4, 4, 4) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE], 1, 1, 1, 1, 1 << 40, 1 << 30) == E.TGC_ERR_INVALID_ARG
+    assert _tg(FAKE, [FAKE] * 2, 2, 1, 1, 1, 1 << 60, 1) == E.TGC_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("shape", [(0, 1, 1, 4, 4), (1, 0, 1, 4, 4), (1, 1, 0, 4, 4), (1, 1, 1, 0, 4), (1, 1, 1, 4, 0)])
@@ -81,6 +86,10 @@ def test_tgather_strided_invalid_and_empty():
     assert L.tgc_tgather_strided(FAKE + 2, good, arr, good, 2, 1, 1, 1, 4, 4, 5, None) == _lib.TGC_ERR_ALIGN
     # empty: returns before looking at any pointer
     assert L.tgc_tgather_strided(None, None, arr, None, 2, 1, 1, 1, 0, 4, 5, None) == _lib.TGC_OK
+    # a view whose last element lies beyond 64-bit byte offsets is refused
+    huge = (ctypes.c_int64 * 5)(1, 1, 1, 1 << 40, 1)
+    assert L.tgc_tgather_strided(FAKE, good, arr, huge, 2, 1, 1, 1, 1 << 24, 4, 5, None) == _lib.TGC_ERR_INVALID_ARG
+    assert L.tgc_tgather_strided(FAKE, huge, arr, good, 2, 1, 1, 1, 1 << 24, 4, 5, None) == _lib.TGC_ERR_INVALID_ARG
 
 
 def test_tgather_ex_rejects_short_dst_and_missing_counters():

@@ -71,6 +71,15 @@ static int elem_size(tgc_dtype dt) {
 
 static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// *acc = *acc * b for non-negative operands, unless the product reaches 2^62: every element
+// count and byte offset the kernels form from it then fits int64 with room to spare.
+static bool mul_fits(int64_t *acc, int64_t b) {
+    int64_t r = 0;
+    if (__builtin_mul_overflow(*acc, b, &r) || r >= (int64_t(1) << 62)) return false;
+    *acc = r;
+    return true;
+}
+
 // Memory pool of the allocating entry point, one per device, owned by the
 // library so that its release threshold does not change the device's default
 // pool.  Up to TGC_POOL_KEEP_BYTES of memory freed back to it stays mapped for
@@ -105,11 +114,16 @@ static int tgather_impl(const tgc_tgather_args &a) {
     if (a.D0 < 0 || a.D1 < 0 || a.D2 < 0 || a.H < 0 || a.W < 0 || a.dst_rows3 < 0) return TGC_ERR_INVALID_ARG;
     const int es = elem_size(a.dtype);
     if (es == 0) return TGC_ERR_DTYPE;
+    if (a.H >= (int64_t(1) << 56)) return TGC_ERR_INVALID_ARG;  // nranks * H must fit
     const int64_t rows3 = a.dst_rows3 == 0 ? (int64_t)a.nranks * a.H : a.dst_rows3;
     if (rows3 < (int64_t)a.nranks * a.H) return TGC_ERR_INVALID_ARG;
     if (a.progress != nullptr && (a.counters == nullptr || a.chunk_rows <= 0)) return TGC_ERR_INVALID_ARG;
-    const int64_t nslab = a.D0 * a.D1 * a.D2;
-    if (nslab == 0 || a.H == 0 || a.W == 0) return TGC_OK;  // empty: early return, nothing written
+    if (a.D0 == 0 || a.D1 == 0 || a.D2 == 0 || a.H == 0 || a.W == 0) return TGC_OK;  // empty: nothing written
+    int64_t nslab = a.D0, dst_bytes = 0;
+    if (!mul_fits(&nslab, a.D1) || !mul_fits(&nslab, a.D2)) return TGC_ERR_INVALID_ARG;
+    dst_bytes = nslab;  // the destination holds every source byte (rows3 >= nranks * H)
+    if (!mul_fits(&dst_bytes, rows3) || !mul_fits(&dst_bytes, a.W) || !mul_fits(&dst_bytes, es))
+        return TGC_ERR_INVALID_ARG;
     if (a.dst == nullptr || a.srcs == nullptr) return TGC_ERR_INVALID_ARG;
     for (int r = 0; r < a.nranks; ++r)
         if (a.srcs[r] == nullptr) return TGC_ERR_INVALID_ARG;
@@ -493,11 +507,29 @@ int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const
     if (D0 < 0 || D1 < 0 || D2 < 0 || H < 0 || W < 0) return TGC_ERR_INVALID_ARG;
     const int es = elem_size(dtype);
     if (es == 0) return TGC_ERR_DTYPE;
-    if (D0 * D1 * D2 * H == 0 || W == 0) return TGC_OK;  // empty: nothing written
+    if (D0 == 0 || D1 == 0 || D2 == 0 || H == 0 || W == 0) return TGC_OK;  // empty: nothing written
     if (dst == nullptr || srcs == nullptr || dst_strides == nullptr || src_strides == nullptr)
         return TGC_ERR_INVALID_ARG;
     for (int k = 0; k < 5; ++k)
         if (dst_strides[k] < 0 || src_strides[k] < 0) return TGC_ERR_INVALID_ARG;
+    // the largest element offset of each view, in bytes, must fit
+    {
+        int64_t rows = nranks;
+        if (!mul_fits(&rows, H)) return TGC_ERR_INVALID_ARG;
+        const int64_t dst_ext[5] = {D0, D1, D2, rows, W}, src_ext[5] = {D0, D1, D2, H, W};
+        for (int v = 0; v < 2; ++v) {
+            const int64_t *ext = v == 0 ? dst_ext : src_ext;
+            const int64_t *str = v == 0 ? dst_strides : src_strides;
+            int64_t last = 0;
+            for (int k = 0; k < 5; ++k) {
+                int64_t term = ext[k] - 1;
+                if (!mul_fits(&term, str[k])) return TGC_ERR_INVALID_ARG;
+                last += term;  // five terms below 2^62 each: no overflow
+                if (last >= (int64_t(1) << 62)) return TGC_ERR_INVALID_ARG;
+            }
+            if (!mul_fits(&last, es)) return TGC_ERR_INVALID_ARG;
+        }
+    }
     for (int r = 0; r < nranks; ++r)
         if (srcs[r] == nullptr) return TGC_ERR_INVALID_ARG;
     if (!aligned(dst, es)) return TGC_ERR_ALIGN;
