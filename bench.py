@@ -60,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--clock-ms", type=int, default=20, help="nvidia-smi sampling period")
     p.add_argument("--pivot", default="auto", choices=["auto", "page", "shard", "none", "ready_queue"],
                    help="tile order of the headline call (auto: the library's choice, as tgc_ag_matmul)")
+    p.add_argument("--tile-n", type=int, default=0, choices=[0, 256, 512],
+                   help="GEMM tile width for the timed calls; 0 = the library's rule")
     p.add_argument("--band-n", type=int, default=0,
                    help="tile raster of the headline call: 0 = the library's choice, > 0 = bands of that many "
                         "tile columns, < 0 = the group raster")
@@ -356,13 +358,17 @@ def run_ours(args, dist: Dist):
     epoch = [0]
     launches = [0]
 
-    def call(mode="fused", delays=True, pivot=args.pivot, out=None, out_format="bf16", band_n=args.band_n):
+    def call(mode="fused", delays=True, pivot=args.pivot, out=None, out_format="bf16", band_n=args.band_n,
+             tile_n=args.tile_n):
         epoch[0] += 1
         tgc.tgc_ag_matmul_ex(shards, B, C if out is None else out, a, cfg.cb, mode=mode, progress=progress,
                              epoch=epoch[0], workspace=ws, order=order if mode == "fused" else None,
                              delay_ns=delay if (mode == "fused" and delays) else None, stream=stream,
-                             pivot=pivot, out_format=out_format, band_n=band_n)
+                             pivot=pivot, out_format=out_format, band_n=band_n, tile_n=tile_n)
         launches[0] += 2 if mode == "unfused" else 1
+
+    plan = tgc.tgc_ag_matmul_plan(shards, B, C, a, cfg.cb, progress=progress, workspace=ws, order=order,
+                                  delay_ns=delay, pivot=args.pivot, band_n=args.band_n, tile_n=args.tile_n)
 
     sampler = ClockSampler(dist.local_rank, args.clock_ms)
     sampler.start()
@@ -385,6 +391,7 @@ def run_ours(args, dist: Dist):
                         + (", seeded release permutation + delays U[0,20us]" if cfg.skewed else ""),
             "M": cfg.M, "N": cfg.N, "K": cfg.K, "R": cfg.R, "comm_block_rows": cfg.cb, "rank": 0,
             "pivot": args.pivot, "band_n": args.band_n,
+            "plan": plan,
             "parallelism": f"replicas x{dist.world} (the path does not shard)",
             "l2": "inputs larger than L2 (shards 4x128 MiB + B 128 MiB); no flush",
             "timing": "CUDA events on the launching stream around exactly `steps` calls, max over ranks",
@@ -396,7 +403,7 @@ def run_ours(args, dist: Dist):
     res["roofline"] = {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peaks["bf16_tflops"],
                        "unit": "TFLOP/s", "frac": round(kernel_tflops / peaks["bf16_tflops"], 4),
                        "traffic": prof, "peak_source": f"{peaks_kind} burst cuBLAS bf16",
-                       "kernel": "ag_gemm_kernel<fused>"}
+                       "kernel": f"ag_gemm_kernel<fused, {plan['tile_n']}-column tiles>"}
 
     if not args.quick:
         # The comparison lines are timed interleaved (rounds of every variant, median per
@@ -471,6 +478,15 @@ def run_ours(args, dist: Dist):
             "note": "context: torch.matmul (cuBLAS) on the gathered A, same shapes, timed right after the "
                     "fused region; the fused figure includes the gather, this one does not"}
         res["sustained"]["fused_over_cublas_gemm"] = round(ms_cb / ms_sus, 4)
+        # the other tile width over a region as long, so that each settles at its own clock
+        other = 256 if plan["tile_n"] == 512 else 512
+        t_ot = [0.0, 0.0]
+        ms_ot = time_device(lambda: call("fused", tile_n=other), n_sus, 3, dist, stream, wall=t_ot)
+        res["sustained"][f"tile_{other}"] = {
+            "value": round(aggregate(ms_ot, flops, dist)[0], 2), "unit": "TFLOP/s", "steps": n_sus,
+            "region_s": round(t_ot[1] - t_ot[0], 3),
+            "note": f"the same fused call on {other}-column tiles, timed right after; the main figure uses "
+                    f"{plan['tile_n']}-column tiles (tile_n = 0: the library's rule)"}
     res["clocks"] = sampler.stop(window=tuple(t_value))
     if "sustained" in res and sampler.lines:
         cs = clock_summary(sampler.lines, tuple(t_sus))
@@ -482,6 +498,11 @@ def run_ours(args, dist: Dist):
             res["sustained"]["cublas_gemm"]["clocks"] = {"sm_mhz": cs["sm_mhz"],
                                                          "samples": cs["samples_in_value_region"],
                                                          "reasons": cs["reasons"]}
+        key = f"tile_{256 if plan['tile_n'] == 512 else 512}"
+        cs = clock_summary(sampler.lines, tuple(t_ot))
+        if cs is not None:
+            res["sustained"][key]["clocks"] = {"sm_mhz": cs["sm_mhz"], "samples": cs["samples_in_value_region"],
+                                               "reasons": cs["reasons"]}
 
     if not args.quick:
         res["other_workloads"] = bench_other_workloads(dev, stream, dist, args, peaks)

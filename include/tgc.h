@@ -289,7 +289,17 @@ typedef enum tgc_out_format {
  *                choice -- for FUSED and FUSED_CE, bands of TGC_DEFAULT_BAND_N
  *                columns when one shard holds fewer whole tile rows (256 rows
  *                each) than group_m, else the group raster; the group raster
- *                for UNFUSED and MM_ONLY.
+ *                for UNFUSED and MM_ONLY.  Band widths count 256-column
+ *                blocks whatever the tile width.
+ *   tile_n       output columns of a GEMM tile: 256 (two TMEM accumulators per
+ *                CTA, so a tile's epilogue overlaps the next tile's MMAs) or 512
+ *                (two 256-column MMA blocks side by side on one accumulator:
+ *                a quarter fewer operand bytes per flop and less power, but the
+ *                epilogue no longer overlaps); 0 = the library's choice: 512
+ *                when K >= 8192 and one shard holds at least group_m tile rows
+ *                (the group raster case), else 256.  Other values are
+ *                TGC_ERR_INVALID_ARG.  The result does not depend on it: every
+ *                element of C is the same chain of 16-deep MMA steps over K.
  *   grid         persistent CTAs (used in pairs); 0 = every SM.
  *   workspace    device memory of tgc_ag_matmul_workspace_bytes() bytes,
  *                128-byte aligned, zero-filled once by the caller before first
@@ -349,6 +359,7 @@ typedef struct tgc_ag_matmul_args {
     tgc_out_format out_format;
     size_t trace_words;
     int band_n;
+    int tile_n;
 } tgc_ag_matmul_args;
 
 int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
@@ -374,9 +385,9 @@ int tgc_ag_matmul_ex(const tgc_ag_matmul_args *args);
 
 /*
  * The tile order and raster a call to tgc_ag_matmul_ex with these arguments runs,
- * with TGC_PIVOT_AUTO and band_n = 0 resolved as described above: pivot is PAGE,
- * SHARD, NONE or READY_QUEUE; band_n > 0 means the band raster of that many tile
- * columns, 0 the group raster of group_m tile rows.  The arguments are checked as
+ * with TGC_PIVOT_AUTO, band_n = 0 and tile_n = 0 resolved as described above: pivot
+ * is PAGE, SHARD, NONE or READY_QUEUE; band_n > 0 means the band raster of bands of
+ * band_n x 256 columns, 0 the group raster of group_m tile rows; tile_n is 256 or 512.  The arguments are checked as
  * tgc_ag_matmul_ex checks them (the same negative status for invalid ones), but
  * nothing is enqueued and no pointer is dereferenced: placeholders will do.  Needs
  * no GPU.
@@ -385,6 +396,7 @@ typedef struct tgc_ag_matmul_plan_t {
     tgc_pivot pivot;
     int band_n;
     int group_m;
+    int tile_n;
 } tgc_ag_matmul_plan_t;
 
 int tgc_ag_matmul_plan(const tgc_ag_matmul_args *args, tgc_ag_matmul_plan_t *out);
@@ -475,22 +487,24 @@ size_t tgc_ag_matmul_workspace_bytes(int nranks, int64_t M, int64_t K, int64_t N
 
 /*
  * Host-side copy of the tile schedule the GEMM kernels run (the same code the
- * device uses).  A tile is tgc_gemm_tile_shape()'s BM x BN outputs, computed
- * by one persistent cluster (a pair of CTAs on two SMs).  Writes, for cluster
- * `cta` of `grid` persistent clusters, the sequence of (pid_m, pid_n) pairs it
- * processes (band_n > 0: band raster of band_n tile columns; band_n <= 0:
- * group raster of group_m tile rows, 0 = 8) into out[2*t], out[2*t+1], at
- * most max_tiles pairs; returns the
- * number of tiles of that cluster, or a negative tgc_status.  Needs no GPU.
- * READY_QUEUE has no static order past its local prefix, and AUTO may choose
- * it: both are TGC_ERR_INVALID_ARG here.
+ * device uses).  A tile is BM x tile_n outputs (BM from tgc_gemm_tile_shape;
+ * tile_n 256 or 512, as tgc_ag_matmul_plan reports for a call), computed by one
+ * persistent cluster (a pair of CTAs on two SMs).  Writes, for cluster `cta` of
+ * `grid` persistent clusters, the sequence of (pid_m, pid_n) pairs it processes
+ * (pid_n counts tiles of tile_n columns; band_n > 0: bands of band_n x 256
+ * columns; band_n <= 0: group raster of group_m tile rows, 0 = 8) into out[2*t],
+ * out[2*t+1], at most max_tiles pairs; returns the number of tiles of that
+ * cluster, or a negative tgc_status.  Needs no GPU.  READY_QUEUE has no static
+ * order past its local prefix, and AUTO may choose it: both are
+ * TGC_ERR_INVALID_ARG here, as is a tile_n other than 256 or 512.
  */
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks,
                                int rank, tgc_pivot pivot, int group_m, int band_n, int grid,
-                               int cta, int64_t *out, int64_t max_tiles);
+                               int cta, int64_t *out, int64_t max_tiles, int tile_n);
 
 /* Tile shape used by the GEMM kernels (BM, BN, BK): BM rows are shared by a
- * pair of CTAs (128 each), BK is the K depth of one pipeline stage. */
+ * pair of CTAs (128 each), BN is the width of one MMA column block (a tile is
+ * one or two blocks wide, see tile_n), BK is the K depth of one pipeline stage. */
 void tgc_gemm_tile_shape(int *bm, int *bn, int *bk);
 
 /* ------------------------------------------------------------------------ */

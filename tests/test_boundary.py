@@ -166,7 +166,7 @@ def _plan(**kw):
     args.update(kw)
     out = _lib.AgMatmulPlan()
     rc = _lib.lib().tgc_ag_matmul_plan(ctypes.byref(_lib.AgMatmulArgs(**args)), ctypes.byref(out))
-    return rc, (out.pivot, out.band_n, out.group_m)
+    return rc, (out.pivot, out.band_n, out.group_m), out.tile_n
 
 
 def test_auto_order_and_raster_follow_the_measured_rule():
@@ -178,23 +178,45 @@ def test_auto_order_and_raster_follow_the_measured_rule():
     square = dict(R=8, M=4096, K=4096, N=4096, comm_block_rows=128)
     mlp_up = dict(R=8, M=8192, K=4096, N=14336, comm_block_rows=256)
     large = dict(R=4, M=32768, K=8192, N=8192, comm_block_rows=512)
-    assert _plan(**square) == (0, (P["page"], 16, 8))
-    assert _plan(**mlp_up) == (0, (P["page"], 16, 8))
-    assert _plan(**large) == (0, (P["page"], 0, 8))
-    assert _plan(**square, order=order, n_order=2) == (0, (P["ready_queue"], 16, 8))
-    assert _plan(**large, order=order, n_order=2) == (0, (P["page"], 0, 8))   # group raster: page
-    assert _plan(**square, group_m=2) == (0, (P["page"], 0, 2))               # 2 tile rows, not < 2
-    assert _plan(**square, band_n=-1) == (0, (P["page"], 0, 8))
-    assert _plan(**large, band_n=5) == (0, (P["page"], 5, 8))
-    assert _plan(**square, mode=_lib.MODES["fused_ce"], order=order, n_order=2) == (0, (P["page"], 16, 8))
+    assert _plan(**square)[:2] == (0, (P["page"], 16, 8))
+    assert _plan(**mlp_up)[:2] == (0, (P["page"], 16, 8))
+    assert _plan(**large)[:2] == (0, (P["page"], 0, 8))
+    assert _plan(**square, order=order, n_order=2)[:2] == (0, (P["ready_queue"], 16, 8))
+    assert _plan(**large, order=order, n_order=2)[:2] == (0, (P["page"], 0, 8))   # group raster: page
+    assert _plan(**square, group_m=2)[:2] == (0, (P["page"], 0, 2))               # 2 tile rows, not < 2
+    assert _plan(**square, band_n=-1)[:2] == (0, (P["page"], 0, 8))
+    assert _plan(**large, band_n=5)[:2] == (0, (P["page"], 5, 8))
+    assert _plan(**square, mode=_lib.MODES["fused_ce"], order=order, n_order=2)[:2] == (0, (P["page"], 16, 8))
     for mode in ("unfused", "mm_only"):
-        assert _plan(**square, mode=_lib.MODES[mode]) == (0, (P["none"], 0, 8))
-        assert _plan(**square, mode=_lib.MODES[mode], pivot=P["ready_queue"]) == (0, (P["none"], 0, 8))
-    assert _plan(**square, pivot=P["shard"]) == (0, (P["shard"], 16, 8))
+        assert _plan(**square, mode=_lib.MODES[mode])[:2] == (0, (P["none"], 0, 8))
+        assert _plan(**square, mode=_lib.MODES[mode], pivot=P["ready_queue"])[:2] == (0, (P["none"], 0, 8))
+    assert _plan(**square, pivot=P["shard"])[:2] == (0, (P["shard"], 16, 8))
     # the same argument checks as the call itself
     assert _plan(**dict(square, M=4097))[0] == _lib.TGC_ERR_INVALID_ARG
+    assert _plan(**dict(square, tile_n=384))[0] == _lib.TGC_ERR_INVALID_ARG
+    assert _plan(**dict(square, tile_n=-256))[0] == _lib.TGC_ERR_INVALID_ARG
     assert _plan(**dict(square, K=60))[0] == _lib.TGC_ERR_ALIGN
     assert _lib.lib().tgc_ag_matmul_plan(None, None) == _lib.TGC_ERR_INVALID_ARG
+
+
+def test_tile_width_follows_the_measured_rule():
+    """tile_n = 0: 512-column tiles when K >= 8192 and a shard holds at least group_m tile rows,
+    in every mode; 256 otherwise; an explicit width is taken as given."""
+    square = dict(R=8, M=4096, K=4096, N=4096, comm_block_rows=128)
+    mlp_up = dict(R=8, M=8192, K=4096, N=14336, comm_block_rows=256)
+    large = dict(R=4, M=32768, K=8192, N=8192, comm_block_rows=512)
+    for mode in ("fused", "fused_ce", "unfused", "mm_only"):
+        m = _lib.MODES[mode]
+        assert _plan(**large, mode=m)[2] == 512, mode
+        assert _plan(**square, mode=m)[2] == 256, mode
+        assert _plan(**mlp_up, mode=m)[2] == 256, mode
+    assert _plan(**dict(large, K=4096))[2] == 256                      # short K
+    assert _plan(**dict(large, R=8, comm_block_rows=256))[2] == 512    # 16 tile rows per shard
+    assert _plan(**dict(large, R=32, comm_block_rows=256))[2] == 256   # 4 tile rows per shard
+    assert _plan(**dict(mlp_up, K=8192))[2] == 256                     # long K, short shards
+    assert _plan(**dict(large, group_m=64))[2] == 256                  # a group longer than a shard
+    assert _plan(**large, tile_n=256)[2] == 256
+    assert _plan(**square, tile_n=512)[2] == 512
 
 
 def test_ag_matmul_empty_problem_is_ok():
@@ -235,8 +257,8 @@ def test_workspace_bytes_grows_with_blocks():
 # ----------------------------------------------------------------------------- schedule
 
 
-def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0, band_n=0):
-    seqs = [tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, pivot, group_m, grid, c, band_n=band_n)
+def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0, band_n=0, tile_n=256):
+    seqs = [tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, pivot, group_m, grid, c, band_n=band_n, tile_n=tile_n)
             for c in range(grid)]
     return seqs
 
@@ -245,11 +267,12 @@ def _all_tiles(M, N, cb, R, rank, pivot, grid, group_m=0, band_n=0):
                                       (64, 64, 8, 4), (1000 * 8, 1000, 1000, 8)])
 @pytest.mark.parametrize("pivot", ["page", "shard", "none"])
 @pytest.mark.parametrize("band_n", [0, 16, 3])
-def test_schedule_is_a_permutation(M, N, cb, R, pivot, band_n):
-    bm, bn, _ = tgc.tgc_gemm_tile_shape()
-    npm, npn = -(-M // bm), -(-N // bn)
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_schedule_is_a_permutation(M, N, cb, R, pivot, band_n, tile_n):
+    bm = tgc.tgc_gemm_tile_shape()[0]
+    npm, npn = -(-M // bm), -(-N // tile_n)
     for rank in sorted({0, 1, R - 1}):
-        seqs = _all_tiles(M, N, cb, R, rank, pivot, grid=148, band_n=band_n)
+        seqs = _all_tiles(M, N, cb, R, rank, pivot, grid=148, band_n=band_n, tile_n=tile_n)
         tiles = [t for s in seqs for t in s]
         assert len(tiles) == npm * npn
         assert len(set(tiles)) == npm * npn
@@ -257,16 +280,17 @@ def test_schedule_is_a_permutation(M, N, cb, R, pivot, band_n):
 
 
 @pytest.mark.parametrize("M,N,cb,R", [(4096, 4096, 512, 8), (32768, 8192, 8192, 4)])
-def test_page_pivot_matches_formula_and_starts_on_local_shard_when_one_block_per_rank(M, N, cb, R):
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_page_pivot_matches_formula_and_starts_on_local_shard_when_one_block_per_rank(M, N, cb, R, tile_n):
     """Triton第四课 (融合后的流水线): pid_m = (pid_m + NUM_PID_M_PER_COMM_BLOCK*RANK) % num_pid_m
     after the GROUP_SIZE_M swizzle; with one comm block per rank every rank begins on its own
     shard."""
-    bm, bn, _ = tgc.tgc_gemm_tile_shape()
-    npm, npn = M // bm, -(-N // bn)
+    bm = tgc.tgc_gemm_tile_shape()[0]
+    npm, npn = M // bm, -(-N // tile_n)
     tpb = cb // bm
     G = 8
     for rank in range(R):
-        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", G, 1, 0)
+        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", G, 1, 0, tile_n=tile_n)
         for t, (pm, pn) in enumerate(seq):
             group = t // (G * npn)
             first = group * G
@@ -279,20 +303,23 @@ def test_page_pivot_matches_formula_and_starts_on_local_shard_when_one_block_per
 
 @pytest.mark.parametrize("M,N,cb,R,band_n", [(8192, 14336, 256, 8, 16), (32768, 8192, 512, 4, 16),
                                              (4096, 4096, 128, 8, 5), (1000 * 8, 1000, 1000, 8, 2)])
-def test_band_raster_walks_rows_in_order_within_each_band(M, N, cb, R, band_n):
-    """Band raster: tiles in bands of band_n tile columns, row-major inside a band, the rank
-    rotation applied to the rows after it; with the page pivot, rank r's walk starts on the row
-    the page's formula gives and every band visits the rows in that rotated order."""
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_band_raster_walks_rows_in_order_within_each_band(M, N, cb, R, band_n, tile_n):
+    """Band raster: tiles in bands of band_n x 256 columns (ceil(band_n x 256 / tile_n) tiles),
+    row-major inside a band, the rank rotation applied to the rows after it; with the page pivot,
+    rank r's walk starts on the row the page's formula gives and every band visits the rows in
+    that rotated order."""
     bm, bn, _ = tgc.tgc_gemm_tile_shape()
-    npm, npn = -(-M // bm), -(-N // bn)
+    npm, npn = -(-M // bm), -(-N // tile_n)
+    bt = -(-band_n * bn // tile_n)  # band width in tiles
     for rank in sorted({0, R - 1}):
-        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", 8, 1, 0, band_n=band_n)
+        seq = tgc.tgc_ag_matmul_schedule(M, N, cb, R, rank, "page", 8, 1, 0, band_n=band_n, tile_n=tile_n)
         assert len(seq) == npm * npn
         off = (rank * cb // bm) % npm
         for t, (pm, pn) in enumerate(seq):
-            band, r = divmod(t, band_n * npm)
-            bw = min(npn - band * band_n, band_n)
-            assert (pm, pn) == ((r // bw + off) % npm, band * band_n + r % bw)
+            band, r = divmod(t, bt * npm)
+            bw = min(npn - band * bt, bt)
+            assert (pm, pn) == ((r // bw + off) % npm, band * bt + r % bw)
 
 
 def test_shard_pivot_starts_every_rank_on_its_shard():
@@ -311,6 +338,9 @@ def test_schedule_rejects_bad_arguments():
         tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 4, "page", 8, 1, 0)
     with pytest.raises(tgc.TGCError):
         tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 0, "page", 8, 2, 2)
+    for width in (0, 128, 1024):
+        with pytest.raises(tgc.TGCError):
+            tgc.tgc_ag_matmul_schedule(64, 64, 8, 4, 0, "page", 8, 1, 0, tile_n=width)
 
 
 def test_trace_word_indices_match_header():

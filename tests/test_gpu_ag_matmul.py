@@ -108,10 +108,11 @@ def test_ragged_shapes_full(R, H, K, N, cb):
     for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue"), ("fused_ce", "page")):
         for rank in sorted({0, R - 1}):
             for band_n in (0, -1, 1):  # default (bands for the fused modes), group raster, one-column bands
-                run.C.zero_()
-                run(mode=mode, rank=rank, pivot=pivot, band_n=band_n)
-                assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank} band {band_n}")
-                assert np.array_equal(bits16(run.a), a_ref)
+                for tile_n in (256, 512):
+                    run.C.zero_()
+                    run(mode=mode, rank=rank, pivot=pivot, band_n=band_n, tile_n=tile_n)
+                    assert_within_tol(run.C, C_ref, f"{mode} {pivot} rank {rank} band {band_n} tile {tile_n}")
+                    assert np.array_equal(bits16(run.a), a_ref)
 
 
 @pytest.mark.parametrize("R,H,K,N", [(4, 16, 64, 64), (2, 128, 64, 512), (4, 96, 128, 248)])
@@ -126,8 +127,10 @@ def test_integer_exact_bitwise(R, H, K, N):
     cfg = AGConfig("int", R=R, H=H, K=K, N=N, cb=H // 2 if H % 2 == 0 else H, b_sigma=1.0)
     run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bi.to(torch.bfloat16))
     for mode in ("fused", "unfused"):
-        run(mode=mode)
-        assert torch.equal(run.C.double().cpu(), ref.double()), mode
+        for tile_n in (256, 512):
+            run.C.zero_()
+            run(mode=mode, tile_n=tile_n)
+            assert torch.equal(run.C.double().cpu(), ref.double()), (mode, tile_n)
 
 
 def test_plain_entry_point_tiny_and_ragged():
@@ -238,6 +241,12 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
     run(mode="fused_ce", **{k: v for k, v in kw.items() if k == "order"})
     assert torch.equal(run.C, C_fused), "copy-engine producer differs"
     assert torch.equal(run.a, torch.cat(run.shards))
+    # both tile widths, whichever the default call took: the same MMA chain for every element
+    for tile_n in (256, 512):
+        for mode in ("fused", "mm_only"):
+            run.C.zero_()
+            run(mode=mode, tile_n=tile_n, **(kw if mode == "fused" else {}))
+            assert torch.equal(run.C, C_fused), (mode, tile_n)
 
 
 # ----------------------------------------------------------------------------- CUDA graphs
@@ -312,9 +321,10 @@ def test_explicit_grid_sizes_give_identical_results():
     ref = run.C.clone()
     for grid in (2, 6, 30):
         for pivot in ("page", "ready_queue"):
-            run.C.zero_()
-            run(grid=grid, pivot=pivot)
-            assert torch.equal(run.C, ref), (grid, pivot)
+            for tile_n in (256, 512):
+                run.C.zero_()
+                run(grid=grid, pivot=pivot, tile_n=tile_n)
+                assert torch.equal(run.C, ref), (grid, pivot, tile_n)
 
 
 def test_trace_records_every_cta():
@@ -327,6 +337,10 @@ def test_trace_records_every_cta():
     assert used.shape[0] >= 2
     # both CTAs of a pair count each 256 x 256 tile they share
     assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
+    trace512 = trace_buffer(_lib.TRACE_WORDS)
+    run(trace=trace512, tile_n=512)   # the same call on 256 x 512 tiles
+    t512 = trace512.view(-1, _lib.TRACE_WORDS).cpu()
+    assert int(t512[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 512)
     # every piece is copied once, by one of the producer warps
     copied = int(used[:, _lib.TRACE["pieces"]].sum())
     assert copied == _expected_pieces(cfg, used)
@@ -412,8 +426,9 @@ def test_fp8_output_integer_exact():
     run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bi.to(torch.bfloat16))
     ref = (torch.cat(si) @ Bi.T).numpy().astype(np.float64)
     for mode, pivot in (("fused", "page"), ("unfused", "page"), ("fused", "ready_queue")):
-        C8 = _run_fp8(run, mode=mode, pivot=pivot)
-        assert np.array_equal(oracle.e4m3_to_f64(C8.cpu().numpy()), ref), mode
+        for tile_n in (256, 512):
+            C8 = _run_fp8(run, mode=mode, pivot=pivot, tile_n=tile_n)
+            assert np.array_equal(oracle.e4m3_to_f64(C8.cpu().numpy()), ref), (mode, tile_n)
 
 
 def test_fp8_output_square_workload_within_one_step():
@@ -465,10 +480,11 @@ def test_stress_random_orders_delays_pivots_bit_exact():
         rank = int(torch.randint(0, cfg.R, (1,), generator=g))
         grid = [0, 2, 8, 40][int(torch.randint(0, 4, (1,), generator=g))]
         band_n = [0, -1, 1, 3][int(torch.randint(0, 4, (1,), generator=g))]
+        tile_n = [0, 256, 512][int(torch.randint(0, 3, (1,), generator=g))]
         run.a.view(torch.int16).fill_(-1)
         run.C.zero_()
-        run(order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n)
-        assert torch.equal(run.C, ref), (i, pivot, rank, grid, band_n)
+        run(order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n, tile_n=tile_n)
+        assert torch.equal(run.C, ref), (i, pivot, rank, grid, band_n, tile_n)
         assert torch.equal(run.a, torch.cat(run.shards)), i
     # status word, ticket dispenser and per-block counters are zero again (the workspace also
     # keeps the device copies of the last order / delay arrays, which need no clearing)
@@ -497,10 +513,11 @@ def test_random_shapes_against_oracle():
         assert_within_tol(run.C, C_ref, f"shape {i}: R={R} H={H} cb={cb} K={K} N={N} unfused")
         for mode, pivot in (("fused", pick(["page", "shard", "ready_queue"])), ("fused_ce", "page")):
             rank = int(torch.randint(0, R, (1,), generator=g))
+            tile_n = pick([256, 512])
             run.a.view(torch.int16).fill_(-1)
             run.C.fill_(float("nan"))
-            run(mode=mode, pivot=pivot, rank=rank)
-            assert torch.equal(run.C, ref), (i, R, H, cb, K, N, mode, pivot, rank)
+            run(mode=mode, pivot=pivot, rank=rank, tile_n=tile_n)
+            assert torch.equal(run.C, ref), (i, R, H, cb, K, N, mode, pivot, rank, tile_n)
             assert np.array_equal(bits16(run.a), a_ref), (i, mode)
 
 
@@ -528,8 +545,10 @@ def test_soak_random_shapes_orders_modes_bit_exact():
             rank = int(torch.randint(0, R, (1,), generator=g))
             grid = pick([0, 2, 16, 64])
             band_n = pick([0, -1, 2, 16])
+            tile_n = pick([0, 256, 512])
             run.a.view(torch.int16).fill_(-1)
             run.C.zero_()
-            run(mode=mode, order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n)
-            assert torch.equal(run.C, ref), (shape_i, it, mode, pivot, rank, grid, band_n)
+            run(mode=mode, order=order, delay_ns=delay, pivot=pivot, rank=rank, grid=grid, band_n=band_n,
+                tile_n=tile_n)
+            assert torch.equal(run.C, ref), (shape_i, it, mode, pivot, rank, grid, band_n, tile_n)
             assert torch.equal(run.a, cat), (shape_i, it)

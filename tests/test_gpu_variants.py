@@ -95,9 +95,10 @@ def test_bulk_producer_matches_unfused_bitwise(use_variant):
     run(mode="unfused")
     ref = run.C.clone()
     for pivot in ("page", "shard", "ready_queue"):
-        run.C.zero_()
-        run(pivot=pivot)
-        assert torch.equal(run.C, ref), pivot
+        for tile_n in (256, 512):
+            run.C.zero_()
+            run(pivot=pivot, tile_n=tile_n)
+            assert torch.equal(run.C, ref), (pivot, tile_n)
     assert torch.equal(run.a, torch.cat(run.shards))
 
 
@@ -146,11 +147,12 @@ def test_cstore_register_copy_ragged_against_oracle(use_cstore, R, H, K, N, cb):
     assert_within_tol(ref, C_ref, "cstore unfused")
     for pivot in ("page", "shard", "ready_queue"):
         for rank in sorted({0, R - 1}):
-            run.C.fill_(float("nan"))
-            run.a.view(torch.int16).fill_(-1)
-            run(pivot=pivot, rank=rank)
-            assert torch.equal(run.C, ref), (pivot, rank)
-            assert np.array_equal(bits16(run.a), a_ref)
+            for tile_n in (256, 512):
+                run.C.fill_(float("nan"))
+                run.a.view(torch.int16).fill_(-1)
+                run(pivot=pivot, rank=rank, tile_n=tile_n)
+                assert torch.equal(run.C, ref), (pivot, rank, tile_n)
+                assert np.array_equal(bits16(run.a), a_ref)
 
 
 def test_cstore_square_workload_sampled_rows(use_cstore):

@@ -6,7 +6,8 @@ include/tgc.h); this package only builds it (``_build``), binds it with ctypes
 plumbing of ranks that are separate processes (``ranks``).
 """
 from ._lib import (  # noqa: F401
-    TGCError, lib, tgc_ag_matmul, tgc_ag_matmul_ex, tgc_ag_matmul_noalloc, tgc_ag_matmul_schedule,
+    TGCError, lib, tgc_ag_matmul, tgc_ag_matmul_ex, tgc_ag_matmul_noalloc, tgc_ag_matmul_plan,
+    tgc_ag_matmul_schedule,
     tgc_ag_matmul_workspace_bytes, tgc_gemm_tile_shape, tgc_ipc_close, tgc_ipc_export, tgc_ipc_open,
     tgc_last_cuda_error, tgc_status_string, tgc_tgather, tgc_tgather_ex, tgc_tgather_strided, tgc_version,
 )

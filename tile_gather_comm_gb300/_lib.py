@@ -65,7 +65,7 @@ class AgMatmulArgs(ctypes.Structure):
         ("spin_timeout_ns", ctypes.c_uint64), ("group_m", ctypes.c_int), ("grid", ctypes.c_int),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("d_status", _vp),
         ("sync", ctypes.c_int), ("stream", _vp), ("trace", _vp), ("out_format", ctypes.c_int),
-        ("trace_words", ctypes.c_size_t), ("band_n", ctypes.c_int),
+        ("trace_words", ctypes.c_size_t), ("band_n", ctypes.c_int), ("tile_n", ctypes.c_int),
     ]
 
 
@@ -75,7 +75,8 @@ class IpcHandle(ctypes.Structure):
 
 
 class AgMatmulPlan(ctypes.Structure):
-    _fields_ = [("pivot", ctypes.c_int), ("band_n", ctypes.c_int), ("group_m", ctypes.c_int)]
+    _fields_ = [("pivot", ctypes.c_int), ("band_n", ctypes.c_int), ("group_m", ctypes.c_int),
+                ("tile_n", ctypes.c_int)]
 
 
 class TGCError(RuntimeError):
@@ -130,7 +131,7 @@ def load_library(path: str) -> ctypes.CDLL:
     L.tgc_ag_matmul_workspace_bytes.restype = ctypes.c_size_t
     L.tgc_ag_matmul_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                         ctypes.POINTER(_i64), _i64]
+                                         ctypes.POINTER(_i64), _i64, ctypes.c_int]
     L.tgc_ag_matmul_schedule.restype = _i64
     L.tgc_gemm_tile_shape.argtypes = [ctypes.POINTER(ctypes.c_int)] * 3
     L.tgc_gemm_tile_shape.restype = None
@@ -272,12 +273,11 @@ def tgc_ag_matmul_workspace_bytes(nranks: int, M: int, K: int, N: int, comm_bloc
     return lib().tgc_ag_matmul_workspace_bytes(nranks, M, K, N, comm_block_rows)
 
 
-def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | None = None, rank: int = 0,
-                     mode: str = "fused", pivot: str = "page", progress=None, epoch: int = 1, order=None,
-                     delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, band_n: int = 0, grid: int = 0,
-                     workspace=None, d_status=None, sync: bool = False, stream=None, trace=None,
-                     out_format: str = "bf16", check: bool = True) -> int:
-    """Extended AllGather-MatMul (see tgc.h).  ``order`` / ``delay_ns`` are host sequences."""
+def _ag_args(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | None = None, rank: int = 0,
+             mode: str = "fused", pivot: str = "page", progress=None, epoch: int = 1, order=None,
+             delay_ns=None, spin_timeout_ns: int = 0, group_m: int = 0, band_n: int = 0, grid: int = 0,
+             workspace=None, d_status=None, sync: bool = False, stream=None, trace=None,
+             out_format: str = "bf16", tile_n: int = 0) -> AgMatmulArgs:
     R = len(a_shards) if a_shards is not None else 1
     K = B.shape[1]
     N = B.shape[0]
@@ -301,19 +301,37 @@ def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, M: int | No
         workspace_bytes=(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         d_status=_ptr(d_status), sync=1 if sync else 0, stream=_stream(stream), trace=_ptr(trace),
         out_format=OUT_FORMATS[out_format],
-        trace_words=(trace.numel() * trace.element_size() // 8) if trace is not None else 0)
+        trace_words=(trace.numel() * trace.element_size() // 8) if trace is not None else 0, tile_n=tile_n)
+    a._keep = (shards, order_arr, delay_arr)  # the host arrays live as long as the struct
+    return a
+
+
+def tgc_ag_matmul_ex(a_shards, B, C, a_out, comm_block_rows: int, *, check: bool = True, **kw) -> int:
+    """Extended AllGather-MatMul (see tgc.h).  ``order`` / ``delay_ns`` are host sequences."""
+    a = _ag_args(a_shards, B, C, a_out, comm_block_rows, **kw)
     rc = lib().tgc_ag_matmul_ex(ctypes.byref(a))
     return _check(rc, "tgc_ag_matmul_ex") if check else rc
 
 
+def tgc_ag_matmul_plan(a_shards, B, C, a_out, comm_block_rows: int, **kw) -> dict:
+    """The tile order, raster and tile width tgc_ag_matmul_ex would run with these arguments."""
+    a = _ag_args(a_shards, B, C, a_out, comm_block_rows, **kw)
+    out = AgMatmulPlan()
+    _check(lib().tgc_ag_matmul_plan(ctypes.byref(a), ctypes.byref(out)), "tgc_ag_matmul_plan")
+    names = {v: k for k, v in PIVOTS.items()}
+    return {"pivot": names.get(out.pivot, out.pivot), "band_n": out.band_n, "group_m": out.group_m,
+            "tile_n": out.tile_n}
+
+
 def tgc_ag_matmul_schedule(M: int, N: int, comm_block_rows: int, nranks: int, rank: int = 0,
-                           pivot: str = "page", group_m: int = 0, grid: int = 1, cta: int = 0, band_n: int = 0):
+                           pivot: str = "page", group_m: int = 0, grid: int = 1, cta: int = 0, band_n: int = 0,
+                           tile_n: int = 256):
     """Tile sequence (pid_m, pid_n) of persistent CTA ``cta`` (host-side copy of the device schedule);
-    ``band_n`` > 0 selects the band raster."""
+    ``band_n`` > 0 selects the band raster; tiles are ``tile_n`` columns wide."""
     n = lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, band_n,
-                                     grid, cta, None, 0)
+                                     grid, cta, None, 0, tile_n)
     _check(int(n) if n < 0 else 0, "tgc_ag_matmul_schedule")
     buf = (_i64 * max(1, 2 * n))()
     lib().tgc_ag_matmul_schedule(M, N, comm_block_rows, nranks, rank, PIVOTS[pivot], group_m, band_n, grid,
-                                 cta, buf, n)
+                                 cta, buf, n, tile_n)
     return [(buf[2 * i], buf[2 * i + 1]) for i in range(n)]

@@ -174,6 +174,7 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     }
     if (a.rank < 0 || a.rank >= a.nranks) return TGC_ERR_INVALID_ARG;
     if (a.group_m < 0 || a.grid < 0) return TGC_ERR_INVALID_ARG;
+    if (a.tile_n != 0 && a.tile_n != 256 && a.tile_n != 512) return TGC_ERR_INVALID_ARG;
     // sizes the kernels index with 32-bit integers
     if (a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 31))
         return TGC_ERR_INVALID_ARG;
@@ -223,8 +224,9 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
 // The tile order and raster a call runs (the resolution of AUTO and of band_n = 0).
 struct OrderPlan {
     int pivot;    // PAGE / SHARD / NONE / READY_QUEUE as the kernel takes it
-    int band_n;   // > 0: band raster of band_n tile columns; 0: group raster
+    int band_n;   // > 0: band raster, bands of band_n x 256 columns; 0: group raster
     int group_m;  // tile rows per group of the group raster
+    int tile_n;   // output columns of a tile: 256 or 512
 };
 
 static OrderPlan resolve_order(const tgc_ag_matmul_args &a, const AGCheck &chk) {
@@ -239,6 +241,13 @@ static OrderPlan resolve_order(const tgc_ag_matmul_args &a, const AGCheck &chk) 
     if (a.band_n > 0) o.band_n = a.band_n;
     else if (a.band_n < 0 || !flagged) o.band_n = 0;
     else o.band_n = chk.rows_per_rank / kTileM < o.group_m ? TGC_DEFAULT_BAND_N : 0;
+    // Tile width.  512 columns read a quarter fewer operand bytes per flop from L2, which
+    // draws less power and lets the capped clock rise, but their single accumulator leaves the
+    // epilogue exposed, and their first wave reaches twice as many tile rows.  They win where
+    // K is long (the epilogue is then a small part of a tile) and a shard's own rows keep the
+    // first waves busy (the group raster's case); 256 elsewhere.
+    if (a.tile_n > 0) o.tile_n = a.tile_n;
+    else o.tile_n = (a.K >= 8192 && chk.rows_per_rank / kTileM >= o.group_m) ? 512 : 256;
     // Tile order.  AUTO: the ready order for FUSED when the caller gives a release order and
     // the band raster walks rows soon enough to meet it out of order; the page's rank pivot
     // otherwise (with the default release order both orders coincide, and the ready order
@@ -401,6 +410,7 @@ static int ag_ex_impl(const tgc_ag_matmul_args &a) {
     const OrderPlan plan = resolve_order(a, chk);
     G.group_m = plan.group_m;
     G.band_n = plan.band_n;
+    G.tile_n = plan.tile_n;
     G.pivot = plan.pivot;
     G.grid = a.grid;
     G.timeout_ns = timeout;
@@ -565,6 +575,7 @@ int tgc_ag_matmul_plan(const tgc_ag_matmul_args *args, tgc_ag_matmul_plan_t *out
     out->pivot = (tgc_pivot)o.pivot;
     out->band_n = o.band_n;
     out->group_m = o.group_m;
+    out->tile_n = o.tile_n;
     return TGC_OK;
 }
 
@@ -631,17 +642,18 @@ int tgc_ag_matmul(const void *const *a_shards, int nranks, const void *B, void *
 
 int64_t tgc_ag_matmul_schedule(int64_t M, int64_t N, int64_t comm_block_rows, int nranks, int rank,
                                tgc_pivot pivot, int group_m, int band_n, int grid, int cta, int64_t *out,
-                               int64_t max_tiles) {
+                               int64_t max_tiles, int tile_n) {
     if (M <= 0 || N <= 0 || nranks <= 0 || M % nranks != 0 || rank < 0 || rank >= nranks || grid <= 0 ||
         cta < 0 || cta >= grid || group_m < 0 || comm_block_rows <= 0)
         return TGC_ERR_INVALID_ARG;
     if (pivot != TGC_PIVOT_PAGE && pivot != TGC_PIVOT_SHARD && pivot != TGC_PIVOT_NONE) return TGC_ERR_INVALID_ARG;  // READY_QUEUE is dynamic
+    if (tile_n != 256 && tile_n != 512) return TGC_ERR_INVALID_ARG;
     TileSchedule s{};
     s.num_pid_m = (int)((M + kTileM - 1) / kTileM);
-    s.num_pid_n = (int)((N + kBN - 1) / kBN);
+    s.num_pid_n = (int)((N + tile_n - 1) / tile_n);
     s.num_tiles = s.num_pid_m * s.num_pid_n;
     s.group_m = group_m > 0 ? group_m : TGC_DEFAULT_GROUP_M;
-    s.band_n = band_n > 0 ? band_n : 0;
+    s.band_n = band_n > 0 ? (int)(((int64_t)band_n * kBN + tile_n - 1) / tile_n) : 0;  // given in 256 columns
     s.pivot_off = pivot_offset((int)pivot, rank, comm_block_rows, M / nranks, kTileM, s.num_pid_m);
     int64_t n = 0;
     for (int t = cta; t < s.num_tiles; t += grid, ++n) {

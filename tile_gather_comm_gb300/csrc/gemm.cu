@@ -64,10 +64,13 @@ namespace tgc {
 
 // Compile-time tuning (defaults chosen by measurement on GB300).
 #ifndef TGC_PAIR_STAGES
-#define TGC_PAIR_STAGES 6        // pipeline stages of the plain GEMM on CTA pairs
+#define TGC_PAIR_STAGES 6        // pipeline stages of the GEMM on CTA pairs, 256-column tiles
 #endif
 #ifndef TGC_PAIR_FUSED_STAGES
-#define TGC_PAIR_FUSED_STAGES 6  // pipeline stages when the copy producer also needs shared memory
+#define TGC_PAIR_FUSED_STAGES 6  // the same when the copy producer also needs shared memory
+#endif
+#ifndef TGC_WIDE_STAGES
+#define TGC_WIDE_STAGES 4        // pipeline stages with 512-column tiles (48 KiB each)
 #endif
 #ifndef TGC_COPY_SLOTS
 #define TGC_COPY_SLOTS 4         // staging slots of the copy producer
@@ -118,14 +121,22 @@ constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns 
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 
 // Per-CTA-group configuration.  CG = number of CTAs sharing one MMA tile.
-template <int CG, bool SLOTS>  // SLOTS: the copy producer's staging slots share shared memory
+// TN: output columns of a tile, 256 (one MMA column block, two TMEM accumulators) or 512
+// (two blocks side by side, one accumulator).
+template <int CG, bool SLOTS, int TN>  // SLOTS: the copy producer's staging slots share shared memory
 struct Cfg {
+    static_assert(TN == 256 || TN == 512, "tile width");
+    static constexpr int kTN = TN;
     static constexpr int kTileM = 128 * CG;             // output rows per (cluster) tile
     static constexpr int kRowsCta = 128;                // rows of A per CTA
-    static constexpr int kHalfN = kBN / CG;             // rows of B (N) each CTA stages
+    static constexpr int kNH = TN / kBN;                // MMA column blocks side by side in a tile
+    static constexpr int kHalfN = kBN / CG;             // rows of B each CTA stages per column block
     static constexpr int kAStage = kRowsCta * kBK * 2;  // 16 KiB
-    static constexpr int kBStage = kHalfN * kBK * 2;    // 32 KiB alone, 16 KiB in a pair
-    static constexpr int kStages = CG == 1 ? 4 : (SLOTS ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
+    static constexpr int kBBox = kHalfN * kBK * 2;      // one column block: 32 KiB alone, 16 KiB in a pair
+    static constexpr int kBStage = kNH * kBBox;
+    static constexpr int kAccs = (int)kTmemCols / TN;   // TMEM accumulators per CTA (2, or 1 at 512)
+    static constexpr int kStages = CG == 1 ? 4 : TN == 512 ? TGC_WIDE_STAGES
+                                                  : (SLOTS ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
     static constexpr uint32_t kIdesc = make_idesc_bf16_f32(kTileM, kBN);
     static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
     static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
@@ -139,18 +150,26 @@ constexpr bool kUsesSlots = FUSED && PROD && !TGC_COPY_LSU;
 // rows x 32 bf16 columns (64 bytes a row, 64-byte swizzle).  The bulk copy
 // producer's slots leave no room for it; that kernel stores C directly.
 constexpr int kCBoxCols = 32, kCBoxRows = 32;
+#ifndef TGC_C_BUFS
+#define TGC_C_BUFS 4  // staging buffers per epilogue warp (TMA stores in flight)
+#endif
+constexpr int kCBufs = TGC_C_BUFS;
+static_assert(kCBufs == 2 || kCBufs == 4, "C staging buffers");
 constexpr int kCBufBytes = kCBoxCols * kCBoxRows * 2;  // 2 KiB
-constexpr int kCStageBytes = 4 * 2 * kCBufBytes;       // 4 warps x 2 buffers
+constexpr int kCStageBytes = 4 * kCBufs * kCBufBytes;  // 4 warps x kCBufs buffers
 template <bool SLOTS>
 constexpr bool kTmaC = TGC_TMA_STORE_C && !SLOTS;
 
-template <int CG, bool SLOTS>
+template <int CG, bool SLOTS, int TN>
 constexpr int smem_bytes() {
-    return 1024 /* alignment slack */ + Cfg<CG, SLOTS>::kStages * (Cfg<CG, SLOTS>::kAStage + Cfg<CG, SLOTS>::kBStage) +
+    using C = Cfg<CG, SLOTS, TN>;
+    return 1024 /* alignment slack */ + C::kStages * (C::kAStage + C::kBStage) +
            (SLOTS ? kSlots * kSlotBytes : 0) + (kTmaC<SLOTS> ? kCStageBytes : 0) + 512 /* barriers + TMEM address */;
 }
 
-static_assert(smem_bytes<2, true>() <= 232448 && smem_bytes<2, false>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<2, true, 256>() <= 232448 && smem_bytes<2, false, 256>() <= 232448 &&
+                  smem_bytes<2, true, 512>() <= 232448 && smem_bytes<2, false, 512>() <= 232448,
+              "shared memory per CTA");
 static_assert((2 * 8 + 4 + kSlots + 1) * 8 + 4 <= 512, "barrier area");
 
 struct GemmParams {
@@ -338,11 +357,11 @@ __device__ __forceinline__ int cluster_id() { return (int)blockIdx.x / CG; }
 template <int CG>
 __device__ __forceinline__ int num_clusters() { return (int)gridDim.x / CG; }
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const CUtensorMap *tmB,
                          const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint32_t crank, int lane) {
-    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>, TN>;
     uint32_t it = 0;
     bool ok = true;
     uint64_t wait_ns = 0, waited_tiles = 0, load_stall_ns = 0;
@@ -363,7 +382,7 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
         }
         const int pid_m = tp.pid_m, pid_n = tp.pid_n;
         const int m0 = pid_m * C::kTileM + (int)crank * C::kRowsCta;  // this CTA's 128 rows
-        const int nb = pid_n * kBN + (int)crank * C::kHalfN;          // this CTA's B rows
+        const int nb = pid_n * C::kTN + (int)crank * C::kHalfN;       // this CTA's B rows (first block)
         const CUtensorMap *mapA = tmA;
         int arow = m0;
         if (FUSED) {
@@ -390,15 +409,23 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
                     mbar_arrive_expect_tx(&full[s], C::kStageTx);
                     if (TGC_A_HINT) tma_load_2d_hint(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow, polA);
                     else tma_load_2d(sA + s * C::kAStage, mapA, &full[s], kb * kBK, arow);
-                    if (TGC_B_HINT) tma_load_2d_hint(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb, polB);
-                    else tma_load_2d(sB + s * C::kBStage, tmB, &full[s], kb * kBK, nb);
+#pragma unroll
+                    for (int h = 0; h < C::kNH; ++h) {
+                        uint8_t *dstB = sB + s * C::kBStage + h * C::kBBox;
+                        if (TGC_B_HINT) tma_load_2d_hint(dstB, tmB, &full[s], kb * kBK, nb + h * kBN, polB);
+                        else tma_load_2d(dstB, tmB, &full[s], kb * kBK, nb + h * kBN);
+                    }
                 } else {
                     if (crank == 0) mbar_arrive_expect_tx(&full[s], C::kStageTx);  // both CTAs' bytes
                     const uint32_t bar = full0 + s * 8u;
                     if (TGC_A_HINT) tma_load_2d_pair_hint(sA + s * C::kAStage, mapA, bar, kb * kBK, arow, polA);
                     else tma_load_2d_pair(sA + s * C::kAStage, mapA, bar, kb * kBK, arow);
-                    if (TGC_B_HINT) tma_load_2d_pair_hint(sB + s * C::kBStage, tmB, bar, kb * kBK, nb, polB);
-                    else tma_load_2d_pair(sB + s * C::kBStage, tmB, bar, kb * kBK, nb);
+#pragma unroll
+                    for (int h = 0; h < C::kNH; ++h) {
+                        uint8_t *dstB = sB + s * C::kBStage + h * C::kBBox;
+                        if (TGC_B_HINT) tma_load_2d_pair_hint(dstB, tmB, bar, kb * kBK, nb + h * kBN, polB);
+                        else tma_load_2d_pair(dstB, tmB, bar, kb * kBK, nb + h * kBN);
+                    }
                 }
             }
         }
@@ -426,11 +453,11 @@ __device__ void role_tma(const CUtensorMap *tmA, const CUtensorMap *tmL, const C
     __syncwarp();
 }
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t *full, uint64_t *empty,
                          uint64_t *tfull, uint64_t *tempty, uint64_t *drain, uint32_t tmem_base, uint32_t crank,
                          int lane) {
-    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>, TN>;
     if (lane == 0 && crank == 0) {  // in a pair only the even CTA issues MMAs
         uint32_t it = 0, tc = 0;
         bool ok = true;
@@ -438,10 +465,10 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
         const bool tr = p.trace != nullptr;
         const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
         for (int t = cluster_id<CG>(); t < p.sched.num_tiles && ok; t += num_clusters<CG>(), ++tc) {
-            const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+            const uint32_t acc = tc % (uint32_t)C::kAccs, aph = (tc / (uint32_t)C::kAccs) & 1u;
             if (!mbar_wait_timed(&tempty[acc], aph ^ 1u, p.status, p.mbar_timeout_ns, tr, &acc_ns)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t d = tmem_base + acc * (uint32_t)kBN;
+            const uint32_t d = tmem_base + acc * (uint32_t)C::kTN;
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                 const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
                 if (!mbar_wait_timed(&full[s], ph, p.status, p.mbar_timeout_ns, tr, &stage_ns)) { ok = false; break; }
@@ -450,10 +477,14 @@ __device__ void role_mma(const GemmParams &p, uint8_t *sA, uint8_t *sB, uint64_t
                 const uint64_t bd = make_sw128_kmajor_desc(b_base + s * C::kBStage);
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
-                    if (CG == 1)
-                        mma_bf16_ss(d, ad + 2u * k, bd + 2u * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
-                    else
-                        mma_bf16_ss_pair(d, ad + 2u * k, bd + 2u * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int h = 0; h < C::kNH; ++h) {  // column block h: accumulator columns h*BN..
+                        const uint64_t bdh = bd + (uint64_t)(h * (C::kBBox >> 4)) + 2u * k;
+                        if (CG == 1)
+                            mma_bf16_ss(d + h * kBN, ad + 2u * k, bdh, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            mma_bf16_ss_pair(d + h * kBN, ad + 2u * k, bdh, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
                 }
                 // frees the stage (in both CTAs of a pair) once these MMAs have read it
                 if (CG == 1) mma_commit(&empty[s]);
@@ -482,13 +513,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                  : "memory");
 }
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8_t *sC, uint64_t *tfull,
                               uint64_t *tempty, uint32_t tmem_base, uint32_t crank, int warp, int lane) {
-    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>, TN>;
     constexpr bool kTma = kTmaC<kUsesSlots<FUSED, PROD>>;
     const bool tma_c = kTma && !p.out_fp8;
-    uint8_t *stg = sC + (warp & 3) * 2 * kCBufBytes;  // this warp's two staging buffers
+    uint8_t *stg = sC + (warp & 3) * kCBufs * kCBufBytes;  // this warp's staging buffers
     uint32_t stores = 0;                              // TMA stores this warp has issued
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -498,7 +529,7 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
     uint64_t epi_ns = 0;
     for (int t = cluster_id<CG>(); t < p.sched.num_tiles; t += num_clusters<CG>(), ++tc) {
         TilePos tp = tile_at(p, t);
-        const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+        const uint32_t acc = tc % (uint32_t)C::kAccs, aph = (tc / (uint32_t)C::kAccs) & 1u;
         bool ok = true;
         if (lane == 0)
             ok = mbar_wait_timed(&tfull[acc], aph, p.status, p.mbar_timeout_ns, p.trace != nullptr, &epi_ns);
@@ -512,14 +543,11 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
         const int pid_m = tp.pid_m, pid_n = tp.pid_n;
         tc_fence_after();
         const int m = pid_m * C::kTileM + (int)crank * C::kRowsCta + row;
-        const int n0 = pid_n * kBN;
+        const int n0 = pid_n * C::kTN;
         uint16_t *crow = p.C + (int64_t)m * p.N;
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)kBN;
-#pragma unroll 1
-        for (int j = 0; j < kBN / 32; ++j) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
-            tmem_wait_ld();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)C::kTN;
+        // Stores one 32-column chunk (fp32 bit patterns in v) of this lane's row to C.
+        auto emit = [&](int j, const uint32_t(&v)[32]) {
             if (p.out_fp8) {
                 // 32 columns -> 32 bytes: two 16-byte stores (N % 16 == 0)
                 if (m < p.M) {
@@ -539,15 +567,15 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
                         }
                     }
                 }
-                continue;
+                return;
             }
             if (kTma && tma_c) {
                 // Row `lane` of a 32 x 32 box goes to shared memory in the 64-byte swizzle
                 // (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)), then one lane stores
                 // the box with TMA; the tensor map clips rows >= M and columns >= N.
-                uint8_t *buf = stg + (stores & 1u) * kCBufBytes;
-                if (stores >= 2) {
-                    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+                uint8_t *buf = stg + (stores % (uint32_t)kCBufs) * kCBufBytes;
+                if (stores >= (uint32_t)kCBufs) {
+                    if (lane == 0) bulk_wait_read<kCBufs - 1>();  // this buffer's previous store has read it
                     __syncwarp();
                 }
 #pragma unroll
@@ -567,7 +595,7 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
                     bulk_commit();
                 }
                 ++stores;
-                continue;
+                return;
             }
             if (m < p.M) {
 #pragma unroll
@@ -583,12 +611,25 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            if (CG == 1) mbar_arrive(&tempty[acc]);
-            else mbar_arrive_cluster(tempty0 + acc * 8u);
+        };
+        // Two chunks per TMEM round trip; the accumulator goes back to the MMA issuer as soon as
+        // its last columns are in registers, before they are converted and stored.
+#pragma unroll 1
+        for (int j = 0; j < C::kTN / 32; j += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v0);
+            tmem_ld_32x32b_x32(taddr + (uint32_t)((j + 1) * 32), v1);
+            tmem_wait_ld();
+            if (j + 2 >= C::kTN / 32) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 1) mbar_arrive(&tempty[acc]);
+                    else mbar_arrive_cluster(tempty0 + acc * 8u);
+                }
+            }
+            emit(j, v0);
+            emit(j + 1, v1);
         }
     }
     if (kTma && lane == 0) bulk_wait<0>();  // every store of C has landed and read its buffer
@@ -860,12 +901,12 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
 
 // ---------------------------------------------------------------- kernel
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                    const GemmParams p) {
-    using C = Cfg<CG, kUsesSlots<FUSED, PROD>>;
+    using C = Cfg<CG, kUsesSlots<FUSED, PROD>, TN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -908,9 +949,9 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        role_tma<CG, FUSED, PROD>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
+        role_tma<CG, FUSED, PROD, TN>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
-        role_mma<CG, FUSED, PROD>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
+        role_mma<CG, FUSED, PROD, TN>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
     } else if (warp == 2 || warp == 3 || warp >= 8) {
         if (FUSED && PROD) {
             if (TGC_COPY_LSU) {
@@ -920,7 +961,7 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
             }
         }
     } else {
-        role_epilogue<CG, FUSED, PROD>(p, &tmC, sC, tfull, tempty, tmem_base, crank, warp, lane);
+        role_epilogue<CG, FUSED, PROD, TN>(p, &tmC, sC, tfull, tempty, tmem_base, crank, warp, lane);
     }
 
     // In a pair, the even CTA's MMAs read the odd CTA's shared memory and write
@@ -998,7 +1039,7 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t col
 constexpr int kCG = 2;
 constexpr int kMaxDevices = 64;
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 static int set_smem_attr(int dev) {
     // a kernel's attributes belong to the device's context: set once per device
     static std::mutex mu;
@@ -1007,15 +1048,15 @@ static int set_smem_attr(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return TGC_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        err[dev] = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem_bytes<CG, kUsesSlots<FUSED, PROD>>());
+        err[dev] = cudaFuncSetAttribute(ag_gemm_kernel<CG, FUSED, PROD, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes<CG, kUsesSlots<FUSED, PROD>, TN>());
         done[dev] = true;
     }
     return err[dev] == cudaSuccess ? TGC_OK : cuda_fail(err[dev]);
 }
 
 // Persistent clusters that can be resident at once (one CTA per SM).
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 static int max_clusters(int dev, int sms) {
     if (CG == 1) return sms;
     static std::mutex mu;
@@ -1031,25 +1072,25 @@ static int max_clusters(int dev, int sms) {
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
         cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>>();
+        cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>, TN>();
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED, PROD>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel<CG, FUSED, PROD, TN>, &cfg) != cudaSuccess || n <= 0)
             n = sms / CG;
         cached[dev] = n;
     }
     return cached[dev];
 }
 
-template <int CG, bool FUSED, bool PROD>
+template <int CG, bool FUSED, bool PROD, int TN>
 static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensorMap &tmB, const CUtensorMap &tmC,
                   const GemmParams &p,
                   int nclusters, cudaStream_t stream) {
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return cuda_fail(de);
-    int rc = set_smem_attr<CG, FUSED, PROD>(dev);
+    int rc = set_smem_attr<CG, FUSED, PROD, TN>(dev);
     if (rc != TGC_OK) return rc;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
@@ -1059,11 +1100,11 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
     cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>>();
+    cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>, TN>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD>, tmA, tmL, tmB, tmC, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ag_gemm_kernel<CG, FUSED, PROD, TN>, tmA, tmL, tmB, tmC, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? TGC_OK : cuda_fail(e);
 }
@@ -1075,7 +1116,7 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
 // time, and a faster copy would only compete with the GEMM's operand loads
 // for HBM.
 static int copy_warps_for(const GemmParams &p, int nclusters) {
-    using C = Cfg<kCG, false>;
+    using C = Cfg<kCG, false, 256>;  // tile rows do not depend on the width
     const int horizon = TGC_COPY_LEAD_WAVES * nclusters;
     bool urgent = false;
     if (p.rq) {
@@ -1113,8 +1154,9 @@ static int piece_bytes_for(const GemmParams &p, int64_t copy_warps_total) {
     return pb;
 }
 
-int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
-    using C = Cfg<kCG, false>;  // tile geometry does not depend on FUSED
+template <int TN>
+static int launch_gemm_tn(const GemmLaunch &L, cudaStream_t stream) {
+    using C = Cfg<kCG, false, TN>;  // tile geometry does not depend on FUSED
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     p.M = (int)L.M;
@@ -1122,10 +1164,11 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     p.K = (int)L.K;
     p.num_kb = (int)((L.K + kBK - 1) / kBK);
     p.sched.num_pid_m = (int)((L.M + C::kTileM - 1) / C::kTileM);
-    p.sched.num_pid_n = (int)((L.N + kBN - 1) / kBN);
+    p.sched.num_pid_n = (int)((L.N + TN - 1) / TN);
     p.sched.num_tiles = p.sched.num_pid_m * p.sched.num_pid_n;
     p.sched.group_m = L.group_m;
-    p.sched.band_n = L.band_n;
+    // band widths are given in columns of one MMA block (256)
+    p.sched.band_n = L.band_n > 0 ? (int)(((int64_t)L.band_n * kBN + TN - 1) / TN) : L.band_n;
     const int64_t rows_per_rank = L.M / L.nranks;
     p.sched.pivot_off = pivot_offset(L.pivot, L.rank, L.cb, rows_per_rank, C::kTileM, p.sched.num_pid_m);
     p.C = static_cast<uint16_t *>(L.C);
@@ -1191,11 +1234,12 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     // persistent clusters: every SM busy; for the plain GEMM no more clusters than tiles
     // (the shared-memory attribute must be set before the occupancy query)
     const int variant = !L.fused ? 0 : (L.producer ? 1 : 2);
-    int rc = variant == 0 ? set_smem_attr<kCG, false, false>(dev)
-           : variant == 1 ? set_smem_attr<kCG, true, true>(dev) : set_smem_attr<kCG, true, false>(dev);
+    int rc = variant == 0 ? set_smem_attr<kCG, false, false, TN>(dev)
+           : variant == 1 ? set_smem_attr<kCG, true, true, TN>(dev) : set_smem_attr<kCG, true, false, TN>(dev);
     if (rc != TGC_OK) return rc;
-    int nclusters = variant == 0 ? max_clusters<kCG, false, false>(dev, sms)
-                  : variant == 1 ? max_clusters<kCG, true, true>(dev, sms) : max_clusters<kCG, true, false>(dev, sms);
+    int nclusters = variant == 0 ? max_clusters<kCG, false, false, TN>(dev, sms)
+                  : variant == 1 ? max_clusters<kCG, true, true, TN>(dev, sms)
+                                 : max_clusters<kCG, true, false, TN>(dev, sms);
     if (L.grid > 0 && L.grid / kCG < nclusters) nclusters = L.grid / kCG;
     if (!L.fused && nclusters > p.sched.num_tiles) nclusters = p.sched.num_tiles;
     if (nclusters < 1) nclusters = 1;
@@ -1206,9 +1250,15 @@ int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
         p.piece_bytes = kMaxPieceBytes;
     }
     if (L.fused) p.pieces_per_block = (int)((p.block_bytes + p.piece_bytes - 1) / p.piece_bytes);
-    return variant == 0 ? launch<kCG, false, false>(tmA, tmL, tmB, tmC, p, nclusters, stream)
-         : variant == 1 ? launch<kCG, true, true>(tmA, tmL, tmB, tmC, p, nclusters, stream)
-                        : launch<kCG, true, false>(tmA, tmL, tmB, tmC, p, nclusters, stream);
+    return variant == 0 ? launch<kCG, false, false, TN>(tmA, tmL, tmB, tmC, p, nclusters, stream)
+         : variant == 1 ? launch<kCG, true, true, TN>(tmA, tmL, tmB, tmC, p, nclusters, stream)
+                        : launch<kCG, true, false, TN>(tmA, tmL, tmB, tmC, p, nclusters, stream);
+}
+
+int launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
+    if (L.tile_n == 512) return launch_gemm_tn<512>(L, stream);
+    if (L.tile_n == 256) return launch_gemm_tn<256>(L, stream);
+    return TGC_ERR_INVALID_ARG;
 }
 
 }  // namespace tgc

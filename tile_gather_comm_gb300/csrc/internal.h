@@ -13,7 +13,7 @@
 
 namespace tgc {
 
-constexpr int kBN = 256;     // GEMM tile cols (tcgen05 N)
+constexpr int kBN = 256;     // columns of one tcgen05.mma (N); a tile is one or two such blocks wide
 constexpr int kBK = 64;      // bf16 elements per 128-byte swizzled row
 constexpr int kTileM = 256;  // GEMM tile rows: a pair of CTAs, 128 rows each (tcgen05 cta_group::2)
 // Fused producer: the unit of the ticket dispenser and of block completion is a
@@ -59,7 +59,8 @@ struct GemmLaunch {
     int rank;
     int pivot;
     int group_m;
-    int band_n;        // > 0: band raster of band_n tile columns; otherwise the group raster
+    int band_n;        // > 0: band raster, bands of band_n x 256 columns; otherwise the group raster
+    int tile_n;        // output columns of a tile: 256 or 512
     int grid;
     uint32_t *progress;
     uint32_t epoch;
