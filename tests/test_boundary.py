@@ -42,7 +42,7 @@ def test_status_strings_and_version():
     assert "wait" in tgc.tgc_status_string(_lib.TGC_ERR_TIMEOUT)
     assert tgc.tgc_status_string(12345) == "unknown status"
     assert tgc.tgc_version().count(".") == 2
-    assert tgc.tgc_gemm_tile_shape() == (256, 256, 64)  # a CTA pair computes 256 x 256
+    assert tgc.tgc_gemm_tile_shape() == (256, 256, 64)  # a CTA pair: 256 rows, 256-column MMA blocks
 
 
 def _tg(dst, srcs, n, D0, D1, D2, H, W, dt=5):

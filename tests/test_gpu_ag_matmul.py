@@ -335,7 +335,7 @@ def test_trace_records_every_cta():
     t = trace.view(-1, _lib.TRACE_WORDS).cpu()
     used = t[t[:, _lib.TRACE["start"]] > 0]
     assert used.shape[0] >= 2
-    # both CTAs of a pair count each 256 x 256 tile they share
+    # both CTAs of a pair count each 256 x 256 tile they share (256-column tiles: K is short here)
     assert int(used[:, _lib.TRACE["tiles"]].sum()) == 2 * (cfg.M // 256) * (cfg.N // 256)
     trace512 = trace_buffer(_lib.TRACE_WORDS)
     run(trace=trace512, tile_n=512)   # the same call on 256 x 512 tiles

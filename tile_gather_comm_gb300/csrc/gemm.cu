@@ -23,20 +23,25 @@
 // order in which the producer completes tile rows.  The host picks the raster
 // and, for TGC_PIVOT_AUTO, the order (api.cu).
 //
-// Tiles are 256 x 256 outputs computed by a CTA pair (a cluster of 2 CTAs on
-// two SMs, tcgen05 cta_group::2): each CTA holds 128 rows of A and 128 of the
-// 256 columns of B per stage, the even CTA issues the 256 x 256 x 16 MMAs for
-// both, and each CTA's TMEM receives its 128 rows of the accumulator.  A
-// single-CTA variant (128 x 256 tiles, cta_group::1) is kept behind the CG
-// template parameter.
+// Tiles are 256 rows by 256 or 512 columns (template parameter TN, chosen per
+// call), computed by a CTA pair (a cluster of 2 CTAs on two SMs, tcgen05
+// cta_group::2): each CTA holds 128 rows of A and, per 256-column block, 128 of
+// the block's columns of B per stage; the even CTA issues the 256 x 256 x 16
+// MMAs for both (two per K step at TN = 512, sharing the A tile), and each CTA's
+// TMEM receives its 128 rows of the accumulator.  At TN = 256 two accumulators
+// alternate, so a tile's epilogue overlaps the next tile's MMAs; at TN = 512 one
+// accumulator fills TMEM, the operand bytes per flop drop by a quarter and the
+// epilogue hands the accumulator back as soon as its last columns are in
+// registers.  A single-CTA variant (128-row tiles, cta_group::1) is kept behind
+// the CG template parameter.
 //
 // CTA anatomy (one CTA per SM, persistent over tiles; 256 threads, 384 for
 // the fused kernel with its extra copy warps):
 //   warp 0     scheduler + flag wait + TMA loads of this CTA's A (128x64) and
-//              B (128x64 per CTA of a pair, 256x64 alone) into a multi-stage
-//              shared-memory ring (128-byte swizzle)
+//              B (128x64 per CTA of a pair and 256-column block, 256x64
+//              alone) into a multi-stage shared-memory ring (128-byte swizzle)
 //   warp 1     TMEM owner; one lane (of the even CTA) issues tcgen05.mma into
-//              one of two TMEM accumulators (2 x 256 fp32 columns)
+//              a TMEM accumulator (2 x 256 or 1 x 512 fp32 columns)
 //   warps 2, 3, 8..11  (FUSED) copy producer: 16-64 KiB pieces of comm blocks,
 //              handed out by a global ticket so any resident CTA can copy any
 //              block, moved with 16-byte register loads and stores (or, with
@@ -45,9 +50,10 @@
 //              flag
 //   warps 4..7 epilogue: tcgen05.ld of the accumulator (one TMEM lane quarter
 //              per warp), fp32 -> bf16 round-to-nearest-even, stores to C
-// The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
-// tile i+1.  All waits are bounded; on expiry the kernel records a status,
-// lets its in-flight copies and MMAs land, frees TMEM and returns.
+// With 256-column tiles the two TMEM accumulators let the epilogue of tile i
+// overlap the mainloop of tile i+1.  All waits are bounded; on expiry the
+// kernel records a status, lets its in-flight copies and MMAs land, frees TMEM
+// and returns.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
