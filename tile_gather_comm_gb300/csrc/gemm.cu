@@ -49,7 +49,9 @@
 //              shared memory); the piece that completes a block publishes its
 //              flag
 //   warps 4..7 epilogue: tcgen05.ld of the accumulator (one TMEM lane quarter
-//              per warp), fp32 -> bf16 round-to-nearest-even, stores to C
+//              per warp), fp32 -> bf16 round-to-nearest-even, stores to C;
+//              with 512-column tiles warps 8..11 are a second epilogue group
+//              for columns 256..511 (and only warps 2, 3 copy)
 // With 256-column tiles the two TMEM accumulators let the epilogue of tile i
 // overlap the mainloop of tile i+1.  All waits are bounded; on expiry the
 // kernel records a status, lets its in-flight copies and MMAs land, frees TMEM
@@ -117,16 +119,28 @@ __device__ __forceinline__ uint64_t make_policy(int kind) {
 constexpr int kThreads = 256;  // warps 0..7: tile loads, MMA, copy (2, 3), epilogue (4..7)
 constexpr int kCopyWarps = TGC_COPY_LSU ? TGC_COPY_WARPS : 1;
 static_assert(kCopyWarps >= 1 && kCopyWarps <= 8, "copy warps");
-// Threads per CTA: the fused kernel with a register copy adds warps 8.. when
-// it runs more than two copy warps.
-template <bool FUSED, bool PROD>
-constexpr int kThreadsOf = (FUSED && PROD && TGC_COPY_LSU && kCopyWarps > 2) ? 32 * (6 + kCopyWarps) : kThreads;
+// Register-copy warps of a kernel: 2 and 3, then 8, 9, ... -- only 2 and 3 with
+// 512-column tiles, whose warps 8..11 are a second epilogue group.
+template <int TN>
+constexpr int kCopyWarpsOf = TN == 512 && kCopyWarps > 2 ? 2 : kCopyWarps;
+// Threads per CTA: the fused kernel with a register copy adds warps 8.. when it
+// runs more than two copy warps; 512-column tiles add warps 8..11 for the
+// epilogue.
+template <bool FUSED, bool PROD, int TN>
+constexpr int kThreadsOf = TN == 512 ? 384
+                         : (FUSED && PROD && TGC_COPY_LSU && kCopyWarps > 2) ? 32 * (6 + kCopyWarps) : kThreads;
 constexpr int kSlots = TGC_COPY_SLOTS;
 constexpr int kSlotBytes = 8192;        // one bulk sub-copy through a staging slot
 constexpr uint32_t kTmemCols = 512;     // two accumulators of 256 fp32 columns x 128 lanes
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 
 // Per-CTA-group configuration.  CG = number of CTAs sharing one MMA tile.
+#ifndef TGC_C_BUFS
+#define TGC_C_BUFS 4  // staging buffers per epilogue warp (TMA stores in flight), 256-column tiles
+#endif
+constexpr int kCBufs = TGC_C_BUFS;
+static_assert(kCBufs == 2 || kCBufs == 4, "C staging buffers");
+
 // TN: output columns of a tile, 256 (one MMA column block, two TMEM accumulators) or 512
 // (two blocks side by side, one accumulator).
 template <int CG, bool SLOTS, int TN>  // SLOTS: the copy producer's staging slots share shared memory
@@ -145,7 +159,9 @@ struct Cfg {
                                                   : (SLOTS ? TGC_PAIR_FUSED_STAGES : TGC_PAIR_STAGES);
     static constexpr uint32_t kIdesc = make_idesc_bf16_f32(kTileM, kBN);
     static constexpr uint32_t kStageTx = CG * (kAStage + kBStage);  // bytes landing per stage
-    static constexpr uint32_t kEpiArrivals = 4 * CG;    // epilogue warps that release an accumulator
+    static constexpr int kEpiGroups = TN == 512 ? 2 : 1;  // groups of 4 epilogue warps, one per 256 columns
+    static constexpr uint32_t kEpiArrivals = 4 * kEpiGroups * CG;  // warps that release an accumulator
+    static constexpr int kCBufsWarp = TN == 512 ? 2 : kCBufs;      // C staging buffers per epilogue warp
 };
 
 // Only the bulk copy producer stages through shared memory.
@@ -156,13 +172,9 @@ constexpr bool kUsesSlots = FUSED && PROD && !TGC_COPY_LSU;
 // rows x 32 bf16 columns (64 bytes a row, 64-byte swizzle).  The bulk copy
 // producer's slots leave no room for it; that kernel stores C directly.
 constexpr int kCBoxCols = 32, kCBoxRows = 32;
-#ifndef TGC_C_BUFS
-#define TGC_C_BUFS 4  // staging buffers per epilogue warp (TMA stores in flight)
-#endif
-constexpr int kCBufs = TGC_C_BUFS;
-static_assert(kCBufs == 2 || kCBufs == 4, "C staging buffers");
 constexpr int kCBufBytes = kCBoxCols * kCBoxRows * 2;  // 2 KiB
-constexpr int kCStageBytes = 4 * kCBufs * kCBufBytes;  // 4 warps x kCBufs buffers
+constexpr int kCStageBytes = 4 * kCBufs * kCBufBytes;  // 4 warps x kCBufs buffers (or 8 x 2 at 512 columns)
+static_assert(kCStageBytes >= 8 * 2 * kCBufBytes, "C staging of the 512-column epilogue");
 template <bool SLOTS>
 constexpr bool kTmaC = TGC_TMA_STORE_C && !SLOTS;
 
@@ -525,7 +537,11 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
     using C = Cfg<CG, kUsesSlots<FUSED, PROD>, TN>;
     constexpr bool kTma = kTmaC<kUsesSlots<FUSED, PROD>>;
     const bool tma_c = kTma && !p.out_fp8;
-    uint8_t *stg = sC + (warp & 3) * kCBufs * kCBufBytes;  // this warp's staging buffers
+    constexpr int kBufs = C::kCBufsWarp;
+    const int ew = warp - 4;                          // index among the epilogue warps
+    const int col0 = (ew >> 2) * kBN;                 // this warp's group's first column of a tile
+    constexpr int kCols = C::kTN / C::kEpiGroups;     // columns of a tile this warp's group stores
+    uint8_t *stg = sC + ew * kBufs * kCBufBytes;      // this warp's staging buffers
     uint32_t stores = 0;                              // TMA stores this warp has issued
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -549,9 +565,9 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
         const int pid_m = tp.pid_m, pid_n = tp.pid_n;
         tc_fence_after();
         const int m = pid_m * C::kTileM + (int)crank * C::kRowsCta + row;
-        const int n0 = pid_n * C::kTN;
+        const int n0 = pid_n * C::kTN + col0;
         uint16_t *crow = p.C + (int64_t)m * p.N;
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)C::kTN;
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)C::kTN + (uint32_t)col0;
         // Stores one 32-column chunk (fp32 bit patterns in v) of this lane's row to C.
         auto emit = [&](int j, const uint32_t(&v)[32]) {
             if (p.out_fp8) {
@@ -579,9 +595,9 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
                 // Row `lane` of a 32 x 32 box goes to shared memory in the 64-byte swizzle
                 // (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)), then one lane stores
                 // the box with TMA; the tensor map clips rows >= M and columns >= N.
-                uint8_t *buf = stg + (stores % (uint32_t)kCBufs) * kCBufBytes;
-                if (stores >= (uint32_t)kCBufs) {
-                    if (lane == 0) bulk_wait_read<kCBufs - 1>();  // this buffer's previous store has read it
+                uint8_t *buf = stg + (stores % (uint32_t)kBufs) * kCBufBytes;
+                if (stores >= (uint32_t)kBufs) {
+                    if (lane == 0) bulk_wait_read<kBufs - 1>();  // this buffer's previous store has read it
                     __syncwarp();
                 }
 #pragma unroll
@@ -621,12 +637,12 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
         // Two chunks per TMEM round trip; the accumulator goes back to the MMA issuer as soon as
         // its last columns are in registers, before they are converted and stored.
 #pragma unroll 1
-        for (int j = 0; j < C::kTN / 32; j += 2) {
+        for (int j = 0; j < kCols / 32; j += 2) {
             uint32_t v0[32], v1[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v0);
             tmem_ld_32x32b_x32(taddr + (uint32_t)((j + 1) * 32), v1);
             tmem_wait_ld();
-            if (j + 2 >= C::kTN / 32) {
+            if (j + 2 >= kCols / 32) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -847,9 +863,10 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4 *ptr) {
 // busy; these copies bypass it.  After its stores every lane fences at gpu
 // scope (and for the async proxy that the consumers' tile loads use); lane 0
 // then retires the piece, and the piece that completes its block publishes it.
+template <int NCW>  // copy warps of the kernel
 __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
-    __shared__ uint32_t s_pieces[kCopyWarps];
-    __shared__ uint64_t s_last[kCopyWarps];
+    __shared__ uint32_t s_pieces[NCW];
+    __shared__ uint64_t s_last[NCW];
     const int cw = warp < 4 ? warp - 2 : warp - 6;  // index among the copy warps
     const uint32_t total = (uint32_t)p.n_order * (uint32_t)p.pieces_per_block;
     const uint64_t t_first = p.trace != nullptr ? globaltimer_ns() : 0;
@@ -888,11 +905,11 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
             s_pieces[cw] = pieces;
             s_last[cw] = globaltimer_ns();
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * kCopyWarps) : "memory");  // the copy warps only
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * NCW) : "memory");  // the copy warps only
         if (cw == 0 && lane == 0) {
             uint64_t last = 0;
             uint32_t sum = 0;
-            for (int i = 0; i < kCopyWarps; ++i) {
+            for (int i = 0; i < NCW; ++i) {
                 last = s_last[i] > last ? s_last[i] : last;
                 sum += s_pieces[i];
             }
@@ -908,7 +925,7 @@ __device__ void role_copy_lsu(const GemmParams &p, int warp, int lane) {
 // ---------------------------------------------------------------- kernel
 
 template <int CG, bool FUSED, bool PROD, int TN>
-__global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
+__global__ void __launch_bounds__(kThreadsOf<FUSED, PROD, TN>, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmL,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                    const GemmParams p) {
@@ -958,10 +975,12 @@ __global__ void __launch_bounds__(kThreadsOf<FUSED, PROD>, 1)
         role_tma<CG, FUSED, PROD, TN>(&tmA, &tmL, &tmB, p, sA, sB, full, empty, crank, lane);
     } else if (warp == 1) {
         role_mma<CG, FUSED, PROD, TN>(p, sA, sB, full, empty, tfull, tempty, drain, tmem_base, crank, lane);
+    } else if (TN == 512 && warp >= 8) {
+        role_epilogue<CG, FUSED, PROD, TN>(p, &tmC, sC, tfull, tempty, tmem_base, crank, warp, lane);
     } else if (warp == 2 || warp == 3 || warp >= 8) {
         if (FUSED && PROD) {
             if (TGC_COPY_LSU) {
-                if (warp < 4 ? warp - 2 < kCopyWarps : true) role_copy_lsu(p, warp, lane);
+                if (warp < 4 ? warp - 2 < kCopyWarpsOf<TN> : true) role_copy_lsu<kCopyWarpsOf<TN>>(p, warp, lane);
             } else if (warp == 2) {
                 role_copy(p, sSlot, slotbar, lane);
             }
@@ -1077,7 +1096,7 @@ static int max_clusters(int dev, int sms) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3((unsigned)(sms / CG * CG), 1, 1);
-        cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
+        cfg.blockDim = dim3(kThreadsOf<FUSED, PROD, TN>, 1, 1);
         cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>, TN>();
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -1105,7 +1124,7 @@ static int launch(const CUtensorMap &tmA, const CUtensorMap &tmL, const CUtensor
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(nclusters * CG), 1, 1);
-    cfg.blockDim = dim3(kThreadsOf<FUSED, PROD>, 1, 1);
+    cfg.blockDim = dim3(kThreadsOf<FUSED, PROD, TN>, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<CG, kUsesSlots<FUSED, PROD>, TN>();
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1251,6 +1270,7 @@ static int launch_gemm_tn(const GemmLaunch &L, cudaStream_t stream) {
     if (nclusters < 1) nclusters = 1;
     if (variant == 1) {
         p.copy_warps = copy_warps_for(p, nclusters);
+        if (p.copy_warps > kCopyWarpsOf<TN>) p.copy_warps = kCopyWarpsOf<TN>;  // the kernel's copy warps
         p.piece_bytes = piece_bytes_for(p, (int64_t)nclusters * kCG * p.copy_warps);
     } else {
         p.piece_bytes = kMaxPieceBytes;
