@@ -105,6 +105,11 @@ namespace tgc {
 #ifndef TGC_TMA_STORE_C
 #define TGC_TMA_STORE_C 1        // bf16 C leaves through shared memory and TMA stores
 #endif
+// 512-column tiles: convert a warp's whole share of the accumulator before
+// handing it back (1), or hand it back after the last TMEM load (0).
+#ifndef TGC_EPI_PACK_ALL
+#define TGC_EPI_PACK_ALL 1
+#endif
 #ifndef TGC_A_HINT
 #define TGC_A_HINT 0             // tile loads of A
 #endif
@@ -634,6 +639,53 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
                 }
             }
         };
+        // 512-column tiles, bf16 C through TMA: the MMA issuer waits for this accumulator, so
+        // the whole of this warp's 256 columns is converted to packed bf16 in registers first
+        // (128 per lane), the accumulator handed back, and only then staged and stored.
+        if (TGC_EPI_PACK_ALL && C::kTN == 512 && kTma && tma_c) {
+            uint32_t pk[kCols / 32][16];
+#pragma unroll
+            for (int j = 0; j < kCols / 32; j += 2) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v0);
+                tmem_ld_32x32b_x32(taddr + (uint32_t)((j + 1) * 32), v1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    pk[j][c] = pack_bf16x2(v0[2 * c], v0[2 * c + 1]);
+                    pk[j + 1][c] = pack_bf16x2(v1[2 * c], v1[2 * c + 1]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (CG == 1) mbar_arrive(&tempty[acc]);
+                else mbar_arrive_cluster(tempty0 + acc * 8u);
+            }
+#pragma unroll
+            for (int j = 0; j < kCols / 32; ++j) {
+                // the box's rows in the 64-byte swizzle, then one TMA store (as in emit)
+                uint8_t *buf = stg + (stores % (uint32_t)kBufs) * kCBufBytes;
+                if (stores >= (uint32_t)kBufs) {
+                    if (lane == 0) bulk_wait_read<kBufs - 1>();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int cs = c ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4 *>(buf + lane * 64 + cs * 16) =
+                        make_uint4(pk[j][4 * c], pk[j][4 * c + 1], pk[j][4 * c + 2], pk[j][4 * c + 3]);
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmC, buf, n0 + j * 32, m - lane);
+                    bulk_commit();
+                }
+                ++stores;
+            }
+            continue;
+        }
         // Two chunks per TMEM round trip; the accumulator goes back to the MMA issuer as soon as
         // its last columns are in registers, before they are converted and stored.
 #pragma unroll 1
