@@ -247,6 +247,20 @@ def clock_summary(lines, window: tuple | None = None):
             "reasons": reasons}
 
 
+def check_device_status(ws, where: str):
+    """The workspace's device status word after a timed region: a bounded wait that expired
+    stops the kernels early, and the times of such calls are not measurements of the work."""
+    import torch
+
+    import tile_gather_comm_gb300 as tgc
+    if ws.is_cuda:
+        torch.cuda.synchronize()
+    st = int(ws[:4].view(torch.int32)[0].item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({tgc.tgc_status_string(st)}) after {where}; "
+                           "the timings of that region are void")
+
+
 def time_interleaved(variants: dict, steps: int, dist: Dist, stream, rounds: int = 6):
     """Median ms per call of each variant, timed in alternating rounds of ~steps/rounds calls."""
     import torch
@@ -378,6 +392,7 @@ def run_ours(args, dist: Dist):
     t_value = [0.0, 0.0]
     ms_fused = time_device(lambda: call("fused"), args.steps, args.warmup, dist, stream, per_step=step_ms,
                            wall=t_value)
+    check_device_status(ws, "the value region")
     fused_launches_timed = args.steps  # one kernel per fused call
     value, ms_max = aggregate(ms_fused, flops, dist)
     kernel_tflops = flops / (ms_fused * 1e-3) * 1e-12
@@ -423,6 +438,7 @@ def run_ours(args, dist: Dist):
         if cfg.skewed:
             variants["no_delay"] = lambda: call("fused", delays=False)
         med = time_interleaved(variants, args.steps, dist, stream)
+        check_device_status(ws, "the comparison lines")
         for k, v in med.items():
             res[k if k != "fused" else "fused_interleaved"] = {
                 "value": round(aggregate(v, flops, dist)[0], 2), "unit": "TFLOP/s",
@@ -455,6 +471,7 @@ def run_ours(args, dist: Dist):
         n_sus = max(args.steps, int(1.2e3 / max(ms_fused, 1e-3)) + 1)
         t_sus = [0.0, 0.0]
         ms_sus = time_device(lambda: call("fused"), n_sus, 3, dist, stream, wall=t_sus)
+        check_device_status(ws, "the sustained region")
         v_sus, ms_sus_max = aggregate(ms_sus, flops, dist)
         k_sus = flops / (ms_sus * 1e-3) * 1e-12
         res["sustained"] = {
@@ -482,6 +499,7 @@ def run_ours(args, dist: Dist):
         other = 256 if plan["tile_n"] == 512 else 512
         t_ot = [0.0, 0.0]
         ms_ot = time_device(lambda: call("fused", tile_n=other), n_sus, 3, dist, stream, wall=t_ot)
+        check_device_status(ws, f"the sustained {other}-column region")
         res["sustained"][f"tile_{other}"] = {
             "value": round(aggregate(ms_ot, flops, dist)[0], 2), "unit": "TFLOP/s", "steps": n_sus,
             "region_s": round(t_ot[1] - t_ot[0], 3),
@@ -581,6 +599,7 @@ def bench_other_workloads(dev, stream, dist, args, peaks):
                                 "fused_ready_queue": lambda: call("fused", "ready_queue"),
                                 "unfused": lambda: call("unfused"), "mm_only": lambda: call("mm_only")},
                                max(args.steps, 300), dist, stream, rounds=10)
+        check_device_status(ws, f"the {name} lines")
         line = {k: round(aggregate(v, float(cfg.flops), dist)[0], 1) for k, v in med.items()}
         line["unit"] = "TFLOP/s"
         line["fused_is"] = "the default call: tile order TGC_PIVOT_AUTO (as tgc_ag_matmul)"
@@ -805,6 +824,7 @@ def bench_e2e(cfg, shards_h, B_h, a, progress, ws, order, delay, dev, stream, di
         step(i)
     torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / steps
+    check_device_status(ws, "the end-to-end region")
     dist.barrier()
     # raw pinned-copy rates on this machine, for context
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -200,14 +200,19 @@ typedef enum tgc_mode {
                               数据搬运与细粒度同步: the backend stream copies every
                               (src_rank, split_id) chunk and then stream_write_value32's
                               its progress entry).  delay_ns is ignored and READY_QUEUE
-                              behaves as PAGE in this mode.  This mode relies on the
-                              device-to-device cudaMemcpyAsync running on the GPU's
-                              copy engines while the persistent GEMM kernel holds
-                              every SM: should the runtime ever carry such a copy out
-                              with a kernel of its own, that kernel could not start
-                              before the GEMM ends, the GEMM's flag waits would expire
-                              and the call would return TGC_ERR_TIMEOUT (after
-                              spin_timeout_ns) instead of a result. */
+                              behaves as PAGE in this mode.  The runtime may carry a
+                              device-to-device cudaMemcpyAsync out with a kernel of its
+                              own rather than a copy engine; that kernel must then find
+                              room on SMs the persistent GEMM kernel already occupies.
+                              So this mode always runs 256-column tiles (256 threads
+                              and about 27 K registers per SM, leaving room for such a
+                              copy kernel beside each GEMM CTA); tile_n = 512 is
+                              TGC_ERR_INVALID_ARG here.  Should the copies still find
+                              no room, the GEMM's flag waits would expire and the call
+                              would return TGC_ERR_TIMEOUT (after spin_timeout_ns)
+                              instead of a result: measured with 512-column tiles,
+                              whose consumer kernel takes 168 registers x 384 threads
+                              of each SM's 65536. */
 } tgc_mode;
 
 /*
@@ -297,8 +302,9 @@ typedef enum tgc_out_format {
  *                a quarter fewer operand bytes per flop and less power, but the
  *                epilogue no longer overlaps); 0 = the library's choice: 512
  *                when K >= 8192 and one shard holds at least group_m tile rows
- *                (the group raster case), else 256.  Other values are
- *                TGC_ERR_INVALID_ARG.  The result does not depend on it: every
+ *                (the group raster case), else 256; always 256 for FUSED_CE (see
+ *                TGC_MODE_FUSED_CE), where 512 is TGC_ERR_INVALID_ARG.  Other
+ *                values are TGC_ERR_INVALID_ARG.  The result does not depend on it: every
  *                element of C is the same chain of 16-deep MMA steps over K.
  *   grid         persistent CTAs (used in pairs); 0 = every SM.
  *   workspace    device memory of tgc_ag_matmul_workspace_bytes() bytes,

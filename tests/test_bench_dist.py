@@ -135,3 +135,15 @@ def test_profiled_traffic_follows_the_kernel_source_hash(tmp_path, monkeypatch):
         assert entry["dram_bytes_per_launch"] > 0, key
         assert os.path.exists(os.path.join(ROOT, "profiles", entry["summary"])), key
         assert entry["command"].startswith("ncu ") and "--clock-control none" in entry["command"], key
+
+
+def test_bench_refuses_timings_of_calls_that_stopped_early():
+    """A bounded device wait that expired leaves its status in the workspace, and the calls after it
+    return at once: the bench must stop rather than report their times as throughput."""
+    import torch
+    import bench
+    ws = torch.zeros(256, dtype=torch.uint8)
+    bench.check_device_status(ws, "a clean region")
+    ws[:4].view(torch.int32)[0] = -6
+    with pytest.raises(RuntimeError, match="bounded device wait"):
+        bench.check_device_status(ws, "a region with a timeout")

@@ -201,15 +201,20 @@ def test_auto_order_and_raster_follow_the_measured_rule():
 
 def test_tile_width_follows_the_measured_rule():
     """tile_n = 0: 512-column tiles when K >= 8192 and a shard holds at least group_m tile rows,
-    in every mode; 256 otherwise; an explicit width is taken as given."""
+    in every mode but FUSED_CE; 256 otherwise; an explicit width is taken as given, except 512
+    with FUSED_CE, which is refused."""
     square = dict(R=8, M=4096, K=4096, N=4096, comm_block_rows=128)
     mlp_up = dict(R=8, M=8192, K=4096, N=14336, comm_block_rows=256)
     large = dict(R=4, M=32768, K=8192, N=8192, comm_block_rows=512)
     for mode in ("fused", "fused_ce", "unfused", "mm_only"):
         m = _lib.MODES[mode]
-        assert _plan(**large, mode=m)[2] == 512, mode
+        # the copy-engine producer keeps 256 columns: its copies may need room on the GEMM's SMs
+        assert _plan(**large, mode=m)[2] == (256 if mode == "fused_ce" else 512), mode
         assert _plan(**square, mode=m)[2] == 256, mode
         assert _plan(**mlp_up, mode=m)[2] == 256, mode
+    assert _plan(**large, mode=_lib.MODES["fused_ce"], tile_n=512)[0] == _lib.TGC_ERR_INVALID_ARG
+    rc, _, width = _plan(**large, mode=_lib.MODES["fused_ce"], tile_n=256)
+    assert (rc, width) == (0, 256)
     assert _plan(**dict(large, K=4096))[2] == 256                      # short K
     assert _plan(**dict(large, R=8, comm_block_rows=256))[2] == 512    # 16 tile rows per shard
     assert _plan(**dict(large, R=32, comm_block_rows=256))[2] == 256   # 4 tile rows per shard

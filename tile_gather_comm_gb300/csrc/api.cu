@@ -175,6 +175,9 @@ int ag_validate(const tgc_ag_matmul_args &a, AGCheck &out) {
     if (a.rank < 0 || a.rank >= a.nranks) return TGC_ERR_INVALID_ARG;
     if (a.group_m < 0 || a.grid < 0) return TGC_ERR_INVALID_ARG;
     if (a.tile_n != 0 && a.tile_n != 256 && a.tile_n != 512) return TGC_ERR_INVALID_ARG;
+    // the copy-engine producer's copies may run as a runtime kernel beside the GEMM CTAs, which
+    // the 512-column kernel (168 registers x 384 threads per SM) leaves no room for
+    if (a.mode == TGC_MODE_FUSED_CE && a.tile_n == 512) return TGC_ERR_INVALID_ARG;
     // sizes the kernels index with 32-bit integers
     if (a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 31))
         return TGC_ERR_INVALID_ARG;
@@ -247,6 +250,7 @@ static OrderPlan resolve_order(const tgc_ag_matmul_args &a, const AGCheck &chk) 
     // K is long (the epilogue is then a small part of a tile) and a shard's own rows keep the
     // first waves busy (the group raster's case); 256 elsewhere.
     if (a.tile_n > 0) o.tile_n = a.tile_n;
+    else if (a.mode == TGC_MODE_FUSED_CE) o.tile_n = 256;  // room for a runtime copy kernel per SM
     else o.tile_n = (a.K >= 8192 && chk.rows_per_rank / kTileM >= o.group_m) ? 512 : 256;
     // Tile order.  AUTO: the ready order for FUSED when the caller gives a release order and
     // the band raster walks rows soon enough to meet it out of order; the page's rank pivot
