@@ -140,6 +140,7 @@ def test_profiled_traffic_follows_the_kernel_source_hash(tmp_path, monkeypatch):
 def test_bench_refuses_timings_of_calls_that_stopped_early():
     """A bounded device wait that expired leaves its status in the workspace, and the calls after it
     return at once: the bench must stop rather than report their times as throughput."""
+    import pytest
     import torch
     import bench
     ws = torch.zeros(256, dtype=torch.uint8)
