@@ -249,6 +249,26 @@ def test_workload_sampled_rows_and_fused_equals_unfused(name):
             assert torch.equal(run.C, C_fused), (mode, tile_n)
 
 
+def test_copy_engine_mode_back_to_back_with_other_modes():
+    """FUSED_CE calls queued back to back behind other modes without a host synchronisation, as a
+    benchmark's interleaved rounds do, on the large workload: the copies, which the runtime may
+    run as a kernel of its own, find room beside the GEMM (the mode keeps 256-column tiles), so no
+    flag wait expires, and C matches the plain GEMM bit for bit."""
+    cfg, shards, B = _inputs("large_skewed")
+    run = Run(cfg, shards, B)
+    run(mode="unfused")   # gathers `a`, then the plain GEMM
+    ref = run.C.clone()
+    run.C.zero_()
+    for mode in ("fused", "mm_only", "fused_ce", "fused_ce", "unfused", "fused_ce", "fused_ce"):
+        run.epoch += 1
+        tgc.tgc_ag_matmul_ex(run.shards, run.B, run.C, run.a, cfg.cb, mode=mode, progress=run.progress,
+                             epoch=run.epoch, workspace=run.ws, sync=False, spin_timeout_ns=500_000_000)
+    torch.cuda.synchronize()
+    assert int(run.ws[:4].view(torch.int32)[0]) == 0, "a bounded wait expired"
+    assert torch.equal(run.C, ref)
+    assert torch.equal(run.a, torch.cat(run.shards))
+
+
 # ----------------------------------------------------------------------------- CUDA graphs
 
 
