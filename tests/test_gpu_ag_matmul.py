@@ -465,6 +465,8 @@ def test_fp8_output_square_workload_within_one_step():
     assert (diff > 0).mean() < 0.01
     C8u = _run_fp8(run, mode="unfused")
     assert torch.equal(C8, C8u), "fused and unfused fp8 outputs differ"
+    C8w = _run_fp8(run, tile_n=512)
+    assert torch.equal(C8, C8w), "256- and 512-column tiles give different fp8 outputs"
 
 
 def test_fp8_output_saturates():
@@ -476,8 +478,9 @@ def test_fp8_output_saturates():
     Bm[: N // 2] *= -1
     cfg = AGConfig("sat", R=R, H=H, K=K, N=N, cb=64, b_sigma=1.0)
     run = Run(cfg, [s.to(torch.bfloat16) for s in si], Bm.to(torch.bfloat16))
-    C8 = _run_fp8(run).cpu().numpy()   # every sum is +-1024
-    assert np.all(C8[:, : N // 2] == 0xFE) and np.all(C8[:, N // 2:] == 0x7E)
+    for tile_n in (256, 512):
+        C8 = _run_fp8(run, tile_n=tile_n).cpu().numpy()   # every sum is +-1024
+        assert np.all(C8[:, : N // 2] == 0xFE) and np.all(C8[:, N // 2:] == 0x7E), tile_n
 
 
 # ----------------------------------------------------------------------------- stress

@@ -686,6 +686,44 @@ __device__ void role_epilogue(const GemmParams &p, const CUtensorMap *tmC, uint8
             }
             continue;
         }
+        // The same for float8 C (32 bytes per 32 columns: 64 words per lane), stored per thread.
+        if (TGC_EPI_PACK_ALL && C::kTN == 512 && p.out_fp8) {
+            uint32_t pk[kCols / 32][8];
+#pragma unroll
+            for (int j = 0; j < kCols / 32; j += 2) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v0);
+                tmem_ld_32x32b_x32(taddr + (uint32_t)((j + 1) * 32), v1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    pk[j][w] = (uint32_t)pack_e4m3x2(v0[4 * w], v0[4 * w + 1]) |
+                               ((uint32_t)pack_e4m3x2(v0[4 * w + 2], v0[4 * w + 3]) << 16);
+                    pk[j + 1][w] = (uint32_t)pack_e4m3x2(v1[4 * w], v1[4 * w + 1]) |
+                                   ((uint32_t)pack_e4m3x2(v1[4 * w + 2], v1[4 * w + 3]) << 16);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (CG == 1) mbar_arrive(&tempty[acc]);
+                else mbar_arrive_cluster(tempty0 + acc * 8u);
+            }
+            if (m < p.M) {
+                uint8_t *crow8 = reinterpret_cast<uint8_t *>(p.C) + (int64_t)m * p.N;
+#pragma unroll
+                for (int j = 0; j < kCols / 32; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int n = n0 + j * 32 + c * 16;  // N % 16 == 0
+                        if (n < p.N)
+                            *reinterpret_cast<uint4 *>(crow8 + n) =
+                                make_uint4(pk[j][4 * c], pk[j][4 * c + 1], pk[j][4 * c + 2], pk[j][4 * c + 3]);
+                    }
+                }
+            }
+            continue;
+        }
         // Two chunks per TMEM round trip; the accumulator goes back to the MMA issuer as soon as
         // its last columns are in registers, before they are converted and stored.
 #pragma unroll 1
