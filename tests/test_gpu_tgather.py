@@ -182,6 +182,31 @@ def test_progress_release_misaligned_views(src_off, dst_off, es):
     assert torch.all(progress == 5) and torch.all(counters == 0)
 
 
+@pytest.mark.parametrize("H,chunk_rows,epochs", [(4096, 128, 1), (3000, 64, 3)])
+def test_progress_release_many_items_per_cta(H, chunk_rows, epochs):
+    """Per-chunk release with far more items than resident CTAs (each CTA walks several items,
+    counting each), over several epochs on the same flags: bytes exact against the oracle,
+    every flag at the last epoch, every counter back at 0."""
+    nranks, D0, W = 8, 2, 1024
+    shape = (D0, 1, 1, H, W)
+    g = torch.Generator().manual_seed(H + chunk_rows)
+    srcs_h = [torch.randint(-2**15, 2**15, shape, generator=g, dtype=torch.int32).to(torch.int16)
+              .view(torch.float16) for _ in range(nranks)]   # random bit patterns, compared as bytes
+    srcs = [s.to(DEV) for s in srcs_h]
+    S = -(-H // chunk_rows)
+    progress = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    counters = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    dst = torch.zeros((D0, 1, 1, nranks * H, W), dtype=torch.float16, device=DEV)
+    ref = oracle.tgather([s.numpy() for s in srcs_h]).tobytes()
+    for e in range(1, epochs + 1):
+        dst.zero_()
+        tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows, epoch=10 + e)
+        torch.cuda.synchronize()
+        assert _bytes(dst) == ref
+        assert torch.all(progress == 10 + e)
+        assert torch.all(counters == 0)
+
+
 @pytest.mark.parametrize("nranks,shape,dtype", [
     (64, (1, 1, 1, 3, 5), torch.int32),       # the maximum rank count
     (64, (2, 1, 1, 17, 128), torch.float16),
