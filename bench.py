@@ -15,7 +15,8 @@ The same JSON line also reports, each timed the same way:
             int32 (1,1,1,1000,777) workload, rotating buffers (> 2 x L2)
   e2e       the fused call with its inputs copied from pinned host memory and
             C copied back inside the timed region
-  cpu_baseline  the CPU oracle on a bounded row sample, host cores
+  cpu_baseline  the CPU oracle on a bounded row sample, host cores (also the
+                TGATHER oracle and the whole square workload's oracle)
 
 ``--impl reference`` times the CPU oracle instead (rank 0 only).
 Multi-GPU: the path does not shard; --gpus N runs N independent replicas
@@ -528,6 +529,7 @@ def run_ours(args, dist: Dist):
         if dist.rank == 0 and dist.world == 1:
             res["cpu_baseline"] = cpu_baseline(cfg, shards_h, B_h)
             res["cpu_baseline_tgather"] = cpu_baseline_tgather(TG_CONFIGS["bw_f16"])
+            res["cpu_baseline_square"] = cpu_baseline_square()
     del shards, B, C, a
     torch.cuda.empty_cache()
     return res
@@ -915,6 +917,42 @@ def cpu_baseline_tgather(tcfg, reps: int = 5):
         oracle.set_num_threads(threads)
     out["single_thread"] = {"value": round(tcfg.bytes_moved / dt1 * 1e-9, 2), "unit": "GB/s", "cores": 1,
                             "seconds": round(dt1, 3), "sample": "one run of the same workload"}
+    return out
+
+
+def cpu_baseline_square():
+    """The AllGather-MatMul oracle on the whole square workload (every row of C), host cores;
+    on one thread, the first 16 rows of C."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from tile_gather_comm_gb300.workloads import AG_CONFIGS, make_ag_inputs
+
+    oracle.build()
+    cfg = AG_CONFIGS["square"]
+    shards_h, B_h = make_ag_inputs(cfg, seed=0)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    sh = [bits(x) for x in shards_h]
+    Bb = bits(B_h)
+    t0 = time.perf_counter()
+    oracle.ag_matmul(sh, Bb)
+    dt = time.perf_counter() - t0
+    out = {"value": round(cfg.flops / dt * 1e-12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "seconds": round(dt, 3),
+           "sample": f"the full square workload: {cfg.R} x ({cfg.H},{cfg.K}) shards, B ({cfg.N},{cfg.K}), every "
+                     f"row of C; fp32 sequential-k dot products, OpenMP over rows"}
+    threads = oracle.num_threads()
+    rows = list(range(16))
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.ag_matmul_rows(sh, Bb, rows)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(threads)
+    out["single_thread"] = {"value": round(2.0 * len(rows) * cfg.N * cfg.K / dt1 * 1e-12, 6), "unit": "TFLOP/s",
+                            "cores": 1, "seconds": round(dt1, 3), "sample": "the first 16 rows of C"}
     return out
 
 
