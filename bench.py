@@ -840,12 +840,31 @@ def bench_e2e(cfg, shards_h, B_h, a, progress, ws, order, delay, dev, stream, di
     e1.record(s_out)
     torch.cuda.synchronize()
     d2h_gbs = d2h / (e0.elapsed_time(e1) * 1e-3) * 1e-9
+    # a step's copies alone, both directions at once (no kernel): the host link's bound on a step
+    both = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        with torch.cuda.stream(s_in):
+            for d, h in zip(sets[0][0], hs):
+                d.copy_(h, non_blocking=True)
+            sets[0][1].copy_(hB, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hC[1].copy_(sets[1][2], non_blocking=True)
+        torch.cuda.synchronize()
+        both.append(time.perf_counter() - t1)
+    both_ms = statistics.median(both) * 1e3
     val, ms_max = aggregate(ms, float(cfg.flops), dist)
     return {"value": round(val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms_max, 3), "steps": steps,
             "call": "tgc_ag_matmul_ex on a compute stream; pinned H2D and D2H on their own streams, "
                     "two device buffer sets (steps overlap)",
-            "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1)}
+            "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+            "copies_only_ms": round(both_ms, 3),
+            "copies_only_gbs": round((h2d + d2h) / (both_ms * 1e-3) * 1e-9, 1),
+            "frac_of_copies_only": round(both_ms / ms_max, 3),
+            "copies_only_note": "one step's H2D and D2H issued together with no kernel (median of 3): the "
+                                "host link's bound on a step on this box, at this time"}
 
 
 def cpu_baseline(cfg, shards_h, B_h, target_rows: int | None = None):
