@@ -37,6 +37,33 @@ def test_exports_every_declared_symbol():
         assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
 
 
+@pytest.mark.parametrize("cls,cname", [(_lib.TgatherArgs, "tgc_tgather_args"),
+                                       (_lib.AgMatmulArgs, "tgc_ag_matmul_args"),
+                                       (_lib.AgMatmulPlan, "tgc_ag_matmul_plan_t"),
+                                       (_lib.IpcHandle, "tgc_ipc_handle")])
+def test_ctypes_structs_match_the_header(cls, cname, tmp_path):
+    """The binding's argument structs have the header's size and every field at the header's
+    offset (a C program compiled against include/tgc.h prints them)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    names = [f[0] for f in cls._fields_]
+    lines = [f'printf("%zu\\n", sizeof({cname}));']
+    lines += [f'printf("%zu\\n", offsetof({cname}, {n}));' for n in names]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"tgc.h\"\nint main(void) {\n"
+                   + "\n".join(lines) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c11", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(cls), cname
+    assert out[1:] == [getattr(cls, n).offset for n in names], cname
+
+
 def test_status_strings_and_version():
     assert tgc.tgc_status_string(0) == "ok"
     assert "wait" in tgc.tgc_status_string(_lib.TGC_ERR_TIMEOUT)

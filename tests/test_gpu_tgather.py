@@ -207,6 +207,37 @@ def test_progress_release_many_items_per_cta(H, chunk_rows, epochs):
         assert torch.all(counters == 0)
 
 
+def test_progress_release_marks_chunks_whose_count_never_completes():
+    """The publisher's wait is bounded: with counters that were not zero on entry (a caller
+    error), no chunk's count ever equals its item count, so after spin_timeout_ns every entry
+    gets ~epoch (never taken for the flag), the rows are still copied, the counters keep what
+    the copying blocks added, and the context stays usable for the next call."""
+    nranks, D0, H, W, chunk_rows = 4, 2, 256, 512, 64
+    shape = (D0, 1, 1, H, W)
+    g = torch.Generator().manual_seed(11)
+    srcs_h = [torch.randint(-2**31, 2**31, shape, generator=g, dtype=torch.int64).to(torch.int32)
+              for _ in range(nranks)]
+    srcs = [s.to(DEV) for s in srcs_h]
+    S = H // chunk_rows
+    progress = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    counters = torch.full((nranks * S,), -2**31, dtype=torch.int32, device=DEV)  # 2^31: never a count
+    dst = torch.zeros((D0, 1, 1, nranks * H, W), dtype=torch.int32, device=DEV)
+    tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows, epoch=7,
+                       spin_timeout_ns=20_000_000)
+    torch.cuda.synchronize()
+    ref = oracle.tgather([s.numpy() for s in srcs_h]).tobytes()
+    assert _bytes(dst) == ref
+    assert torch.all(progress == ~7)
+    assert torch.all(counters > -2**31)   # every chunk was counted on top of the bad start
+    # the same flags, cleared, then a correct call: published as usual
+    counters.zero_()
+    dst.zero_()
+    tgc.tgc_tgather_ex(dst, srcs, progress=progress, counters=counters, chunk_rows=chunk_rows, epoch=8)
+    torch.cuda.synchronize()
+    assert _bytes(dst) == ref
+    assert torch.all(progress == 8) and torch.all(counters == 0)
+
+
 @pytest.mark.parametrize("nranks,shape,dtype", [
     (64, (1, 1, 1, 3, 5), torch.int32),       # the maximum rank count
     (64, (2, 1, 1, 17, 128), torch.float16),

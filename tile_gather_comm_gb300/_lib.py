@@ -49,7 +49,7 @@ class TgatherArgs(ctypes.Structure):
         ("D0", _i64), ("D1", _i64), ("D2", _i64), ("H", _i64), ("W", _i64),
         ("dtype", ctypes.c_int), ("dst_rows3", _i64),
         ("progress", _vp), ("counters", _vp), ("chunk_rows", _i64),
-        ("epoch", ctypes.c_uint32), ("stream", _vp),
+        ("epoch", ctypes.c_uint32), ("stream", _vp), ("spin_timeout_ns", ctypes.c_uint64),
     ]
 
 
@@ -217,12 +217,13 @@ def tgc_tgather_strided(dst, srcs, stream=None, check: bool = True) -> int:
 
 
 def tgc_tgather_ex(dst, srcs, dst_rows3: int = 0, progress=None, counters=None, chunk_rows: int = 0,
-                   epoch: int = 0, stream=None, check: bool = True) -> int:
+                   epoch: int = 0, stream=None, spin_timeout_ns: int = 0, check: bool = True) -> int:
     D0, D1, D2, H, W = srcs[0].shape
     arr = _ptrs(srcs)
     a = TgatherArgs(dst=_ptr(dst), srcs=arr, nranks=len(srcs), D0=D0, D1=D1, D2=D2, H=H, W=W,
                     dtype=DTYPES[srcs[0].dtype], dst_rows3=dst_rows3, progress=_ptr(progress),
-                    counters=_ptr(counters), chunk_rows=chunk_rows, epoch=epoch, stream=_stream(stream))
+                    counters=_ptr(counters), chunk_rows=chunk_rows, epoch=epoch, stream=_stream(stream),
+                    spin_timeout_ns=spin_timeout_ns)
     rc = lib().tgc_tgather_ex(ctypes.byref(a))
     return _check(rc, "tgc_tgather_ex") if check else rc
 

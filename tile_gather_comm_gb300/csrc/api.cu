@@ -147,6 +147,7 @@ static int tgather_impl(const tgc_tgather_args &a) {
         L.progress = a.progress;
         L.counters = a.counters;
         L.epoch = a.epoch;
+        L.spin_timeout_ns = a.spin_timeout_ns;
     } else {
         L.seg_bytes = L.run_bytes;
         L.nseg = 1;

@@ -39,6 +39,7 @@ struct TGatherLaunch {
     uint32_t *progress;
     uint32_t *counters;
     uint32_t epoch;
+    uint64_t spin_timeout_ns;  // the publisher's bound (0: default)
 };
 int launch_tgather(const TGatherLaunch &L, cudaStream_t stream);
 int launch_tgather_strided(const void *const *srcs, void *dst, int nranks, int64_t D0, int64_t D1, int64_t D2,

@@ -67,6 +67,13 @@ __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+// Release reduction without a returned value: the writes that precede it (this thread's, and
+// through a barrier the CTA's) are visible before the add, and the thread does not wait for
+// the add to reach memory.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

@@ -61,6 +61,11 @@ namespace tgc {
 #define TGC_TG_REL_ATOM 1      // release kernel: thread 0 counts an item with one release atomic (1),
                                // or with a gpu-scope fence followed by an acq_rel atomic (0)
 #endif
+#ifndef TGC_TG_REL_POLL
+#define TGC_TG_REL_POLL 1      // release kernel: copying CTAs count items with a release reduction that
+                               // returns nothing and CTA 0 publishes each completed chunk (1), or the
+                               // CTA whose returned count completes a chunk publishes it (0)
+#endif
 #ifndef TGC_TG_CHUNK
 #define TGC_TG_CHUNK 32768     // flat kernel: shares above this many bytes are cut into chunks
                                // dealt round-robin over the CTAs (0: one contiguous share each)
@@ -84,6 +89,7 @@ struct TGParams {
     uint32_t *progress;
     uint32_t *counters;
     uint32_t epoch;
+    uint64_t publish_timeout_ns;  // publisher CTA's bound on waiting for a chunk's count
 };
 
 struct alignas(32) Vec32 { uint32_t w[8]; };
@@ -131,6 +137,34 @@ __device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t
     }
 }
 
+// CTA 0 of the release kernel with a publisher: publishes each chunk once all its items are
+// counted.  Thread t watches chunks t, t + kTGThreads, ... in turn (items are chunk-major, so
+// chunks complete in about that order) with gpu-scope acquire loads: the value that completes
+// the count was written by the last of a chain of release adds, so every counted item's bytes
+// are visible to the thread, which then resets the counter and stores `epoch` with a release.
+// The copying CTAs never wait, so the counts always complete while the GPU runs the grid; the
+// wait is still bounded: a chunk not counted within publish_timeout_ns of the start gets
+// ~epoch (never equal to epoch) in its progress entry instead, and its counter is left as is.
+__device__ __forceinline__ void tg_publish(const TGParams &p, int tid) {
+    const uint32_t target = (uint32_t)(p.nslab * p.tiles_per_seg);
+    const int64_t nch = (int64_t)p.nranks * p.nseg;
+    const uint64_t t0 = globaltimer_ns();
+    bool late = false;
+    for (int64_t c = tid; c < nch; c += kTGThreads) {
+        uint32_t spins = 0;
+        while (!late && ld_acquire_gpu(p.counters + c) != target) {
+            if ((++spins & 15u) == 0 && globaltimer_ns() - t0 > p.publish_timeout_ns) late = true;
+            else __nanosleep(128);
+        }
+        if (late) {
+            st_relaxed_gpu(p.progress + c, ~p.epoch);
+            continue;
+        }
+        st_relaxed_gpu(p.counters + c, 0u);  // every item of this chunk is counted
+        st_release_gpu(p.progress + c, p.epoch);
+    }
+}
+
 template <int VW>
 __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
     using V = typename VecT<VW>::T;
@@ -141,8 +175,16 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     const int tid = threadIdx.x;
+    const bool poll = TGC_TG_REL_POLL && p.progress != nullptr;
+    if (poll && blockIdx.x == 0) {
+        tg_publish(p, tid);
+        return;
+    }
+    // with a publisher, CTAs 1.. copy
+    const int64_t first = poll ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
+    const int64_t step = poll ? (int64_t)gridDim.x - 1 : (int64_t)gridDim.x;
 
-    for (int64_t item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+    for (int64_t item = first; item < p.total_items; item += step) {
         // item = ((s * nranks + r) * nslab + slab) * tiles_per_seg + tile
         const int64_t tile = item % p.tiles_per_seg;
         int64_t rest = item / p.tiles_per_seg;
@@ -186,11 +228,14 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
         }
 
         if (p.progress != nullptr) {
-            // Publish chunk (r, s) once all its nslab*tiles_per_seg items are written.  The
+            // Count the item towards chunk (r, s), whose nslab*tiles_per_seg items publish it.  The
             // barrier orders every thread's stores of this item before thread 0's count; the other
             // threads go on to their next item instead of each waiting for its own stores.
             __syncthreads();
-            if (tid == 0) {
+            if (tid == 0 && poll) {
+                // counted without waiting for the add to land: CTA 0 publishes the chunk
+                red_add_release_gpu(p.counters + ((int64_t)r * p.nseg + s), 1u);
+            } else if (tid == 0) {
                 const int64_t c = (int64_t)r * p.nseg + s;
                 const uint32_t target = (uint32_t)(p.nslab * p.tiles_per_seg);
 #if TGC_TG_REL_ATOM
@@ -453,6 +498,7 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     p.progress = L.progress;
     p.counters = L.counters;
     p.epoch = L.epoch;
+    p.publish_timeout_ns = L.spin_timeout_ns > 0 ? L.spin_timeout_ns : 10000000000ull;
 
     const int vw = pick_vw(L);
     const int64_t tile_vecs = (int64_t)kTGThreads * (vw == 32 ? kTGUnroll / 2 : kTGUnroll);  // the kernel's kTileVecs
@@ -504,7 +550,8 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
         return e == cudaSuccess ? TGC_OK : cuda_fail(e);
     }
     const int64_t waves = (p.total_items + slots - 1) / slots;
-    const int64_t grid = (p.total_items + waves - 1) / waves;
+    int64_t grid = (p.total_items + waves - 1) / waves;
+    if (TGC_TG_REL_POLL && L.progress != nullptr) ++grid;  // CTA 0 publishes
 
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
