@@ -66,6 +66,9 @@ namespace tgc {
                                // returns nothing and CTA 0 publishes each completed chunk (1), or the
                                // CTA whose returned count completes a chunk publishes it (0)
 #endif
+#ifndef TGC_TG_PUBLISH_SLEEP_NS
+#define TGC_TG_PUBLISH_SLEEP_NS 128  // release kernel: the publisher's pause between polls of a count
+#endif
 #ifndef TGC_TG_CHUNK
 #define TGC_TG_CHUNK 32768     // flat kernel: shares above this many bytes are cut into chunks
                                // dealt round-robin over the CTAs (0: one contiguous share each)
@@ -139,7 +142,7 @@ __device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t
 
 // CTA 0 of the release kernel with a publisher: publishes each chunk once all its items are
 // counted.  Thread t watches chunks t, t + kTGThreads, ... in turn (items are chunk-major, so
-// chunks complete in about that order) with gpu-scope acquire loads: the value that completes
+// chunks complete in about that order) with gpu-scope acquire loads, TGC_TG_PUBLISH_SLEEP_NS apart: the value that completes
 // the count was written by the last of a chain of release adds, so every counted item's bytes
 // are visible to the thread, which then resets the counter and stores `epoch` with a release.
 // The copying CTAs never wait, so the counts always complete while the GPU runs the grid; the
@@ -154,7 +157,7 @@ __device__ __forceinline__ void tg_publish(const TGParams &p, int tid) {
         uint32_t spins = 0;
         while (!late && ld_acquire_gpu(p.counters + c) != target) {
             if ((++spins & 15u) == 0 && globaltimer_ns() - t0 > p.publish_timeout_ns) late = true;
-            else __nanosleep(128);
+            else if (TGC_TG_PUBLISH_SLEEP_NS > 0) __nanosleep(TGC_TG_PUBLISH_SLEEP_NS);
         }
         if (late) {
             st_relaxed_gpu(p.progress + c, ~p.epoch);
