@@ -11,19 +11,20 @@
 // Without progress release (tgather_flat_kernel) each CTA of a grid of 8 per SM
 // copies an equal byte share of the concatenated runs.  With progress release
 // (tgather_kernel) each run is cut into segments, one per progress chunk, each
-// segment into tiles of kTGThreads*kTGUnroll vectors, and a persistent grid
-// walks the (segment, tile) items.  Copies go through registers with VW-byte vectors
+// segment into tiles of kTGThreads*kTGUnroll vectors, and the grid's CTAs walk
+// the (segment, tile) items.  Copies go through registers with VW-byte vectors
 // (16 bytes whenever the source and destination agree modulo 16), coalesced:
 // consecutive threads touch consecutive vectors.  The unaligned head and the
 // ragged tail of a segment (fewer than VW bytes each) are copied element by
 // element by the segment's first tile -- this replaces the page's dynamic
 // ValidRow/ValidCol masks, so any H and W work.
 //
-// Per-chunk release: when progress is given, the CTA that finishes the last
-// tile of chunk (r, s) -- counted with an acq_rel atomic -- stores `epoch`
-// into progress[r*S + s] with st.release.gpu ("Triton第四课：基于对称内存融合
-// AllGather 与 MatMul，提速1.56倍", section 数据搬运与细粒度同步: data visible
-// before the flag).
+// Per-chunk release: when progress is given, every item of chunk (r, s) is
+// counted with a gpu-scope release reduction once its bytes are stored, and
+// CTA 0 stores `epoch` into progress[r*S + s] with st.release.gpu once the
+// chunk's count is complete ("Triton第四课：基于对称内存融合 AllGather 与
+// MatMul，提速1.56倍", section 数据搬运与细粒度同步: data visible before the
+// flag).
 #include <cstdint>
 #include <cuda_runtime.h>
 
