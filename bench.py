@@ -662,7 +662,7 @@ def bench_tgather_strided(tcfg, dev, dist, peaks, peaks_kind, pad: int = 64):
                      "traffic": profiled_traffic(f"tgather_strided/{tcfg.name}", TGATHER_SOURCES),
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_strided_rows_kernel<32>"},
     }
-    del sets, graphs
+    del sets, g
     return out
 
 
@@ -729,7 +729,7 @@ def bench_tgather_release(tcfg, dev, dist, peaks, peaks_kind, chunk_rows: int = 
                      "traffic": profiled_traffic(f"tgather_release/{tcfg.name}", TGATHER_SOURCES),
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_kernel<16>"},
     }
-    del sets, g
+    del sets, graphs
     return out
 
 

@@ -138,14 +138,16 @@ int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const
  *              paragraph: versioned progress values keep a previous round's
  *              flag from passing as a new one).
  *   spin_timeout_ns  (with progress) bound on the kernel's one wait, 0 = 10 s.
- *              The copying blocks count each piece of a chunk and never wait;
- *              one block publishes every chunk whose count is complete, and
- *              waits for the counts.  Those always complete while the GPU runs
- *              the grid, but should a chunk's count not complete within this
- *              bound (for example, counters that were not zero on entry), its
- *              entry receives ~epoch instead of epoch (an error mark no reader
- *              takes for the flag) and its counter is left as it is; its rows
- *              are still copied.
+ *              With up to 512 chunks (nranks*S), the copying blocks count each
+ *              piece of a chunk and never wait; one block publishes every chunk
+ *              whose count is complete, and waits for the counts.  Those always
+ *              complete while the GPU runs the grid, but should a chunk's count
+ *              not complete within this bound (for example, counters that were
+ *              not zero on entry), its entry receives ~epoch instead of epoch
+ *              (an error mark no reader takes for the flag) and its counter is
+ *              left as it is; its rows are still copied.  With more chunks the
+ *              block whose count completes a chunk publishes it, nothing waits,
+ *              and this bound is unused.
  */
 typedef struct tgc_tgather_args {
     void *dst;

@@ -20,11 +20,12 @@
 // ValidRow/ValidCol masks, so any H and W work.
 //
 // Per-chunk release: when progress is given, every item of chunk (r, s) is
-// counted with a gpu-scope release reduction once its bytes are stored, and
-// CTA 0 stores `epoch` into progress[r*S + s] with st.release.gpu once the
-// chunk's count is complete ("Triton第四课：基于对称内存融合 AllGather 与
-// MatMul，提速1.56倍", section 数据搬运与细粒度同步: data visible before the
-// flag).
+// counted with a gpu-scope release add once its bytes are stored, and
+// `epoch` goes into progress[r*S + s] with st.release.gpu once the chunk's
+// count is complete ("Triton第四课：基于对称内存融合 AllGather 与 MatMul，
+// 提速1.56倍", section 数据搬运与细粒度同步: data visible before the flag) --
+// stored by CTA 0, which watches the counts, for up to 512 chunks, else by the
+// CTA whose add (returning the count) completes the chunk.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -67,6 +68,10 @@ namespace tgc {
                                // returns nothing and CTA 0 publishes each completed chunk (1), or the
                                // CTA whose returned count completes a chunk publishes it (0)
 #endif
+#ifndef TGC_TG_PUBLISH_MAX_CHUNKS
+#define TGC_TG_PUBLISH_MAX_CHUNKS 512  // publisher only up to this many chunks (two per publisher thread):
+                                       // it publishes a thread's chunks one after another, one poll each
+#endif
 #ifndef TGC_TG_PUBLISH_SLEEP_NS
 #define TGC_TG_PUBLISH_SLEEP_NS 128  // release kernel: the publisher's pause between polls of a count
 #endif
@@ -94,6 +99,7 @@ struct TGParams {
     uint32_t *counters;
     uint32_t epoch;
     uint64_t publish_timeout_ns;  // publisher CTA's bound on waiting for a chunk's count
+    int publish;                  // 1: CTA 0 publishes the chunks, the others count without waiting
 };
 
 struct alignas(32) Vec32 { uint32_t w[8]; };
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kTGThreads) tgather_kernel(const TGParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     const int tid = threadIdx.x;
-    const bool poll = TGC_TG_REL_POLL && p.progress != nullptr;
+    const bool poll = p.publish != 0;  // set by the host only with progress
     if (poll && blockIdx.x == 0) {
         tg_publish(p, tid);
         return;
@@ -555,7 +561,11 @@ int launch_tgather(const TGatherLaunch &L, cudaStream_t stream) {
     }
     const int64_t waves = (p.total_items + slots - 1) / slots;
     int64_t grid = (p.total_items + waves - 1) / waves;
-    if (TGC_TG_REL_POLL && L.progress != nullptr) ++grid;  // CTA 0 publishes
+    // CTA 0 publishes when the chunks are few enough for its threads to watch them without
+    // falling behind; otherwise the CTA whose count completes a chunk publishes it
+    p.publish = TGC_TG_REL_POLL && L.progress != nullptr &&
+                (int64_t)L.nranks * L.nseg <= (int64_t)TGC_TG_PUBLISH_MAX_CHUNKS;
+    if (p.publish) ++grid;
 
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
