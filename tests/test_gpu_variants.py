@@ -12,9 +12,10 @@ library under the package's build folder and checked like the default build:
   does).
 
 A second build keeps the default register-copy producer and turns only the
-per-thread C stores on, together with the TGATHER release kernel's earlier
-form (a gpu-scope fence then an acq_rel count per item, no programmatic
-dependent launch), so that each of those paths is run on its own.
+per-thread C stores on, together with the TGATHER release kernel's earliest
+form (no publisher block at any chunk count: the block whose count completes
+a chunk publishes it, each count a gpu-scope fence then an acq_rel add; no
+programmatic dependent launch), so that each of those paths is run on its own.
 
 Results must be identical to the oracle (TGATHER bit for bit, GEMM within the
 tolerance, bit for bit on integer-exact inputs) and to the default build's
@@ -37,7 +38,7 @@ from .test_gpu_ag_matmul import Run, _custom, _expected_pieces, _inputs, _oracle
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 VARIANT = {"TGC_COPY_LSU": 0, "TGC_TG_CHUNK": 0, "TGC_TG_VW32": 0, "TGC_TMA_STORE_C": 0}
-VARIANT_CSTORE = {"TGC_TMA_STORE_C": 0, "TGC_TG_REL_ATOM": 0, "TGC_TG_REL_PDL": 0}
+VARIANT_CSTORE = {"TGC_TMA_STORE_C": 0, "TGC_TG_REL_ATOM": 0, "TGC_TG_REL_PDL": 0, "TGC_TG_REL_POLL": 0}
 
 
 @pytest.fixture(scope="module")
@@ -166,7 +167,8 @@ def test_cstore_square_workload_sampled_rows(use_cstore):
 
 @pytest.mark.parametrize("H,W,chunk_rows,D0", [(1024, 1024, 128, 2), (1000, 777, 96, 1)])
 def test_cstore_build_release_kernel_bit_exact(use_cstore, H, W, chunk_rows, D0):
-    """The TGATHER release kernel's earlier form (fence, then an acq_rel count per item)."""
+    """The TGATHER release kernel's earliest form (the completing block publishes; fence, then an
+    acq_rel count per item)."""
     nranks = 8
     shape = (D0, 1, 1, H, W)
     g = torch.Generator().manual_seed(H * W)
