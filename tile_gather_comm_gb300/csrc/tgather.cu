@@ -149,9 +149,10 @@ __device__ __forceinline__ void copy_elems(uint8_t *d, const uint8_t *s, int64_t
 
 // CTA 0 of the release kernel with a publisher: publishes each chunk once all its items are
 // counted.  Thread t watches chunks t, t + kTGThreads, ... in turn (items are chunk-major, so
-// chunks complete in about that order) with gpu-scope acquire loads, TGC_TG_PUBLISH_SLEEP_NS apart: the value that completes
-// the count was written by the last of a chain of release adds, so every counted item's bytes
-// are visible to the thread, which then resets the counter and stores `epoch` with a release.
+// chunks complete in about that order) with gpu-scope acquire loads, TGC_TG_PUBLISH_SLEEP_NS
+// apart: the value that completes the count was written by the last of a chain of release adds,
+// so every counted item's bytes are visible to the thread, which then resets the counter and
+// stores `epoch` with a release.
 // The copying CTAs never wait, so the counts always complete while the GPU runs the grid; the
 // wait is still bounded: a chunk not counted within publish_timeout_ns of the start gets
 // ~epoch (never equal to epoch) in its progress entry instead, and its counter is left as is.
