@@ -218,6 +218,9 @@ def tgc_tgather_strided(dst, srcs, stream=None, check: bool = True) -> int:
 
 def tgc_tgather_ex(dst, srcs, dst_rows3: int = 0, progress=None, counters=None, chunk_rows: int = 0,
                    epoch: int = 0, stream=None, spin_timeout_ns: int = 0, check: bool = True) -> int:
+    """TGATHER with the extended arguments of tgc_tgather_args: a taller destination
+    (``dst_rows3``) and per-chunk progress release (``progress``, ``counters``, ``chunk_rows``,
+    ``epoch``, ``spin_timeout_ns``), as include/tgc.h describes them.  Asynchronous on ``stream``."""
     D0, D1, D2, H, W = srcs[0].shape
     arr = _ptrs(srcs)
     a = TgatherArgs(dst=_ptr(dst), srcs=arr, nranks=len(srcs), D0=D0, D1=D1, D2=D2, H=H, W=W,
