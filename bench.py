@@ -334,7 +334,7 @@ def run_ours(args, dist: Dist):
 
     import tile_gather_comm_gb300 as tgc
     from tile_gather_comm_gb300 import _build
-    from tile_gather_comm_gb300.workloads import (AG_CONFIGS, TG_CONFIGS, TGConfig, make_ag_inputs,
+    from tile_gather_comm_gb300.workloads import (AG_CONFIGS, TG_CONFIGS, make_ag_inputs,
                                                   make_release_schedule, make_tg_inputs)
 
     _build.build()
@@ -354,6 +354,7 @@ def run_ours(args, dist: Dist):
                                                   peaks_kind, args)
         res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
+        res["tgather_context_long"] = bench_tgather_context_long(dev, stream, dist, peaks, peaks_kind, args)
         return res
     cfg = AG_CONFIGS[args.workload]
     flops = float(cfg.flops)
@@ -459,12 +460,7 @@ def run_ours(args, dist: Dist):
         res["tgather"] = bench_tgather(TG_CONFIGS["bw_f16"], dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_ragged_i32"] = bench_tgather(TG_CONFIGS["ragged_i32"], dev, stream, dist, peaks,
                                                   peaks_kind, args)
-        # context: the same kernel on 8x taller sources, where the per-launch start and drain
-        # (about 2 us, fixed) weigh 8x less
-        long_cfg = TGConfig("bw_f16_long", 8, (2, 1, 1, 8192, 1024), torch.float16, "normal")
-        res["tgather_context_long"] = bench_tgather(long_cfg, dev, stream, dist, peaks, peaks_kind, args)
-        res["tgather_context_long"]["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the "
-                                               "TGATHER workload; per-launch start and drain amortised")
+        res["tgather_context_long"] = bench_tgather_context_long(dev, stream, dist, peaks, peaks_kind, args)
         res["tgather_strided"] = bench_tgather_strided(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         res["tgather_release"] = bench_tgather_release(TG_CONFIGS["bw_f16"], dev, dist, peaks, peaks_kind)
         # the same fused call over a region of at least a second: the GPU settles at its power
@@ -778,6 +774,20 @@ def bench_tgather(tcfg, dev, stream, dist, peaks, peaks_kind, args):
                      "peak_source": f"{peaks_kind} STREAM-style copy", "kernel": "tgather_flat_kernel<32>"},
     }
     del sets, g
+    return out
+
+
+def bench_tgather_context_long(dev, stream, dist, peaks, peaks_kind, args):
+    """Context line: the TGATHER kernel on 8x taller sources, where the per-launch start and
+    drain (about 2 us, fixed) weigh 8x less."""
+    import torch
+
+    from tile_gather_comm_gb300.workloads import TGConfig
+
+    long_cfg = TGConfig("bw_f16_long", 8, (2, 1, 1, 8192, 1024), torch.float16, "normal")
+    out = bench_tgather(long_cfg, dev, stream, dist, peaks, peaks_kind, args)
+    out["note"] = ("context only: 8 x fp16 (2,1,1,8192,1024), 8x the rows of the TGATHER workload; "
+                   "per-launch start and drain amortised")
     return out
 
 
