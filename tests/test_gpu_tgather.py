@@ -209,6 +209,30 @@ def test_progress_release_many_items_per_cta(H, chunk_rows, epochs):
         assert torch.all(counters == 0)
 
 
+@pytest.mark.parametrize("chunk_rows", [16, 1])   # 64 chunks (publisher block), 1024 (completing block)
+def test_progress_release_with_taller_destination(chunk_rows):
+    """Per-chunk release into a destination with DIM_3 > nranks*H ([TG] §7.2): the gathered rows
+    exact, the rows past them in every slab untouched, every flag published."""
+    nranks, D0, H, W = 8, 3, 128, 96
+    shape = (D0, 1, 1, H, W)
+    g = torch.Generator().manual_seed(chunk_rows)
+    srcs = [torch.randint(-2**31, 2**31, shape, generator=g, dtype=torch.int64).to(torch.int32)
+            for _ in range(nranks)]
+    rows3 = nranks * H + 37
+    prefill = np.full((D0, 1, 1, rows3, W), -5, dtype=np.int32)
+    dst = torch.from_numpy(prefill.copy()).to(DEV)
+    S = -(-H // chunk_rows)
+    progress = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    counters = torch.zeros(nranks * S, dtype=torch.int32, device=DEV)
+    tgc.tgc_tgather_ex(dst, [s.to(DEV) for s in srcs], dst_rows3=rows3, progress=progress, counters=counters,
+                       chunk_rows=chunk_rows, epoch=4)
+    torch.cuda.synchronize()
+    ref = oracle.tgather([s.numpy() for s in srcs], dst_rows3=rows3, dst=prefill)
+    assert _bytes(dst) == ref.tobytes()
+    assert torch.all(dst[:, :, :, nranks * H:] == -5)
+    assert torch.all(progress == 4) and torch.all(counters == 0)
+
+
 def test_progress_release_marks_chunks_whose_count_never_completes():
     """The publisher's wait is bounded: with counters that were not zero on entry (a caller
     error), no chunk's count ever equals its item count, so after spin_timeout_ns every entry
