@@ -117,8 +117,7 @@ int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const
 
 /*
  * Extended TGATHER.  Zero-initialise the struct (`tgc_tgather_args a = {0};`):
- * a zero field takes its default, and fields added at the end of the struct
- * in later versions keep their defaults for such callers.  Adds:
+ * every field below means its default at 0 or a null pointer.  Adds:
  *   dst_rows3  dst's DIM_3; 0 means nranks*H.  [TG] §7.2: it may exceed
  *              nranks*H, in which case only the first nranks*H rows of each
  *              (d0, d1, d2) slab are written and the rest are left unchanged.
@@ -273,8 +272,9 @@ typedef enum tgc_out_format {
 
 /*
  * Extended AllGather-MatMul.  Zero-initialise the struct, as for
- * tgc_tgather_args: a zero field takes its default.  Fields beyond
- * tgc_ag_matmul's:
+ * tgc_tgather_args; each field's description below says what 0 or a null
+ * pointer means (pivot 0 is TGC_PIVOT_PAGE, not the plain call's AUTO).
+ * Fields beyond tgc_ag_matmul's:
  *   a_out        device (M, K) bf16: the gathered A.  FUSED and UNFUSED write
  *                it completely (local shard included); MM_ONLY reads it.
  *   rank         the calling virtual rank, 0 <= rank < nranks.  Tiles whose
