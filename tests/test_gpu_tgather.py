@@ -136,7 +136,8 @@ def test_empty_leaves_dst(shape):
 
 @pytest.mark.parametrize("H,W,chunk_rows,D0", [(1024, 1024, 128, 2), (1000, 777, 96, 1), (64, 32, 7, 3),
                                                (1024, 64, 8, 2),    # 1024 chunks: the counting CTAs publish
-                                               (300, 40, 1, 1)])    # 2400 one-row chunks
+                                               (300, 40, 1, 1),     # 2400 one-row chunks
+                                               (5, 3, 8, 1)])       # chunk_rows > H: one chunk per rank
 def test_progress_release(H, W, chunk_rows, D0):
     nranks = 8
     shape = (D0, 1, 1, H, W)
