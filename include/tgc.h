@@ -116,7 +116,8 @@ int tgc_tgather_strided(void *dst, const int64_t *dst_strides, const void *const
                         tgc_dtype dtype, cudaStream_t stream);
 
 /*
- * Extended TGATHER.  Zero-initialise the struct (`tgc_tgather_args a = {0};`):
+ * Extended TGATHER.  Zero-initialise the struct (`tgc_tgather_args a = {0};`,
+ * `tgc_tgather_args a{};` in C++):
  * every field below means its default at 0 or a null pointer.  Adds:
  *   dst_rows3  dst's DIM_3; 0 means nranks*H.  [TG] §7.2: it may exceed
  *              nranks*H, in which case only the first nranks*H rows of each

@@ -64,6 +64,24 @@ def test_ctypes_structs_match_the_header(cls, cname, tmp_path):
     assert out[1:] == [getattr(cls, n).offset for n in names], cname
 
 
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_compiles_cleanly_as_c_and_cpp(lang, tmp_path):
+    """include/tgc.h is a C header usable from C11 and C++17 with strict warnings as errors."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("compiler or CUDA headers not available")
+    src = tmp_path / ("h.c" if lang == "c" else "h.cpp")
+    init = "= {0}" if lang == "c" else "{}"   # zero-initialised, as the header asks
+    src.write_text('#include "tgc.h"\nint main(void) { tgc_tgather_args a ' + init + '; tgc_ag_matmul_args b '
+                   + init + '; (void)a; (void)b; return TGC_OK; }\n')
+    std = "-std=c11" if lang == "c" else "-std=c++17"
+    subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-isystem", cuda_inc, "-c", str(src), "-o", str(tmp_path / "h.o")], check=True)
+
+
 def test_status_strings_and_version():
     assert tgc.tgc_status_string(0) == "ok"
     assert "wait" in tgc.tgc_status_string(_lib.TGC_ERR_TIMEOUT)
